@@ -1,0 +1,81 @@
+"""Oracle model of one tensor's scaling state across training steps.
+
+TEST INFRASTRUCTURE ONLY (tests, smoke check, benchmark CPU baseline).
+
+Follows "Practice c06/E3, worked solution": the statistic is the largest |x|
+of the tensor, watched over a window of steps; the scale is the largest power
+of two keeping that window maximum at or below the format's largest finite
+value divided by 2^margin; the previous scale is kept under a hysteresis rule.
+The gist.science summary of "Max-Window Scale Estimation for Near-Lossless HiF8
+W8A8 QAT" (Methodology, "Amax algorithms") names the variants: most-recent
+(window 1), max over a history window (64 there), and current tensor scaling.
+
+Readings adopted where the pages are silent:
+  * the window holds the amaxes of the W steps *before* this one; this step's
+    amax enters it after the cast;
+  * an empty window (first step, or W = 0) means current scaling: the
+    exponent comes from this tensor's own amax (a second pass);
+  * a zero or non-finite window maximum keeps the previous exponent (0 when
+    there is none);
+  * hysteresis h (in binades, 0 = off): an upward move of at most h binades
+    keeps the previous exponent; a downward move is always taken, so the
+    no-overflow promise of the worked solution is never delayed;
+  * the exponent is clamped to [-126, 126] so that 2^e and 2^-e are normal
+    fp32 numbers.
+"""
+from __future__ import annotations
+
+import struct
+
+import numpy as np
+
+from . import coracle
+
+
+def f32_of_bits(b: int) -> float:
+    return struct.unpack("<f", struct.pack("<I", b & 0xFFFFFFFF))[0]
+
+
+def bits_of_f32(v: float) -> int:
+    return struct.unpack("<I", struct.pack("<f", v))[0]
+
+
+class ScalingState:
+    """One tensor's history ring, previous exponent and policy."""
+
+    def __init__(self, fmt: int, window: int, margin: int = 0, hysteresis: int = 0):
+        self.fmt, self.window, self.margin, self.hysteresis = fmt, window, margin, hysteresis
+        self.hist: list[int] = []          # amax bit patterns, oldest first
+        self.prev_e: int | None = None
+        self.steps = 0
+
+    def uses_current(self) -> bool:
+        return self.window == 0 or not self.hist
+
+    def exponent(self, window_amax_bits: int) -> int:
+        e_new = coracle.scale_exp(window_amax_bits, self.fmt, self.margin)
+        if e_new is None:                               # zero or non-finite
+            return self.prev_e if self.prev_e is not None else 0
+        if (self.prev_e is not None and e_new > self.prev_e
+                and e_new - self.prev_e <= self.hysteresis):
+            return self.prev_e
+        return e_new
+
+    def step(self, x: np.ndarray, nthreads: int = 1):
+        """Cast one step's tensor x (raw bits).  Returns
+        (q, amax_bits, scale_inv_bits, clipped, e)."""
+        if self.uses_current():
+            a_w = coracle.amax(x, nthreads)
+        else:
+            a_w = max(self.hist)
+        e = self.exponent(a_w)
+        q, a_cur, clipped = coracle.cast(x, self.fmt, e, nthreads)
+        self.record(a_cur, e)
+        return q, a_cur, bits_of_f32(2.0 ** -e), clipped, e
+
+    def record(self, amax_bits: int, e: int):
+        if self.window > 0:
+            self.hist.append(amax_bits)
+            del self.hist[:-self.window]
+        self.prev_e = e
+        self.steps += 1

@@ -1,0 +1,102 @@
+"""Pins of the oracle's MX cast ("what actually breaks low precision
+training", "What the measurements said": blocks of 32 share a power of two
+from the OCP formula, which puts the block's largest value where the 8-bit
+format cannot fully reach it, so the biggest values clip; one extra bit of
+exponent headroom fixes it)."""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import spec
+
+EMAX = {0: 8, 1: 15}
+
+
+@pytest.mark.parametrize("f", [0, 1])
+@pytest.mark.parametrize("h", [0, 1])
+def test_mx_exp_all_bf16_amax_vs_frexp(f, h, orc):
+    """E = floor(log2 A) - emax_elem + h for every positive finite bf16 A,
+    floor(log2) taken from math.frexp (exact), clamped to [-127, 127]."""
+    for b in range(1, 0x7F80):
+        a = spec.f32_bits_exact(b << 16)[1]
+        m, p = math.frexp(float(a))
+        want = max(-127, min(127, (p - 1) - EMAX[f] + h))
+        assert orc.mx_exp(b << 16, f, h) == want
+        if b % 61 == 0:
+            assert spec.mx_exp([spec.E4M3, spec.E5M2][f], a, h) == want
+    assert orc.mx_exp(0, f, h) == -127
+
+
+def _bf16(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bits, round to nearest even (plain integer arithmetic)."""
+    b = x.astype(np.float32).view(np.uint32).astype(np.uint64)
+    r = ((b >> 16) & 1) + 0x7FFF
+    return ((b + r) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("f", [0, 1])
+def test_ocp_rule_puts_block_max_in_top_binade(f, orc):
+    """Under the OCP rule the scaled block maximum lies in
+    [2^emax, 2^(emax+1)): above fmax = 1.75 * 2^emax for part of that range,
+    which is why the biggest values clip."""
+    rng = np.random.default_rng(21)
+    x = _bf16(rng.standard_normal((64, 256)) * np.exp(rng.uniform(-20, 20, size=(64, 1))))
+    q, e8, _ = orc.mx_cast(x, f, 0)
+    xf = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    blocks = np.abs(xf).reshape(-1, 32).max(axis=1)
+    scaled = blocks * 2.0 ** -(e8.reshape(-1).astype(np.int64) - 127)
+    assert np.all((scaled >= 2.0 ** EMAX[f]) & (scaled < 2.0 ** (EMAX[f] + 1)))
+
+
+@pytest.mark.parametrize("f", [0, 1])
+def test_headroom_removes_clipping(f, orc):
+    """One extra bit of exponent headroom: zero clipped for any finite input
+    whose block exponent is not clamped; the OCP rule clips on the same
+    tanh-like data (values piled up just under 1.0)."""
+    rng = np.random.default_rng(22)
+    x = _bf16(np.tanh(rng.standard_normal((128, 512)) * 2.0))
+    _, _, clipped_ocp = orc.mx_cast(x, f, 0)
+    _, _, clipped_h1 = orc.mx_cast(x, f, 1)
+    assert clipped_h1 == 0
+    if f == 0:
+        assert clipped_ocp > 0
+
+
+def test_mx_spec_vs_c_small(orc):
+    """Exact specification and C oracle agree byte for byte on small
+    tensors with zeros, subnormals, NaN/Inf blocks and huge blocks."""
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((6, 64)) * np.exp(rng.uniform(-30, 30, size=(6, 1)))
+    x[0, :32] = 0.0
+    x[0, 3] = -0.0
+    x[1, 5] = np.nan
+    x[2, 40] = -np.inf
+    x[3, :32] *= 1e-38                      # bf16 subnormals
+    x[4, 32:] = 3e38
+    xb = _bf16(x)
+    vals = [spec.bf16_bits_exact(int(b)) for b in xb.reshape(-1)]
+    for f, sf in ((0, spec.E4M3), (1, spec.E5M2)):
+        for h in (0, 1, 2):
+            q, e8, clipped = orc.mx_cast(xb, f, h)
+            qs, e8s, clipped_s = spec.mx_cast_tensor(sf, vals, 64, h)
+            assert list(q.reshape(-1)) == qs
+            assert list(e8.reshape(-1)) == e8s
+            assert clipped == clipped_s
+    q, e8, _ = orc.mx_cast(xb, 0, 0)
+    assert e8[0, 0] == 0 and np.all(q[0, :32] & 0x7F == 0) and q[0, 3] == 0x80
+    assert e8[1, 0] == 0xFF and np.all(q[1, :32] & 0x7F == 0x7F)
+    assert e8[2, 1] == 0xFF
+
+
+def test_mx_layout_row_blocks(orc):
+    """Blocks run along the last dimension: permuting whole blocks of a row
+    permutes the E8M0 bytes the same way; transposing does not commute."""
+    rng = np.random.default_rng(24)
+    x = _bf16(rng.standard_normal((4, 128)) * np.array([[1], [100], [1e-3], [7]]))
+    q, e8, _ = orc.mx_cast(x, 0, 0)
+    perm = [2, 0, 3, 1]
+    xp = x.reshape(4, 4, 32)[:, perm, :].reshape(4, 128)
+    qp, e8p, _ = orc.mx_cast(xp, 0, 0)
+    assert np.array_equal(e8p, e8[:, perm])
+    assert np.array_equal(qp.reshape(4, 4, 32), q.reshape(4, 4, 32)[:, perm, :])
