@@ -1,0 +1,196 @@
+/*
+ * fp8q.h -- C ABI of libfp8q, a GB300 (sm_103a) library for the scaled cast
+ * of training tensors to 8-bit floats.
+ *
+ * What it computes, and where the pages define it:
+ *  - Formats ("Mixed Precision FP16/BF16/FP8" mind-map card, bit layouts and
+ *    ranges, item 3): OCP E4M3 (4 exponent + 3 mantissa bits, largest finite
+ *    448) for weights and activations, OCP E5M2 (5 + 2, largest finite 57344)
+ *    for gradients.
+ *  - Per-tensor scale ("Practice c06/E3", worked solution): watch the largest
+ *    |x| of a tensor over a window of steps; the scale is the largest power
+ *    of two keeping that value at or below the format's largest finite value
+ *    divided by 2^margin; keep the previous scale under a hysteresis rule.
+ *  - Window variants (gist.science summary of "Max-Window Scale Estimation
+ *    for Near-Lossless HiF8 W8A8 QAT", Methodology, "Amax algorithms"):
+ *    most-recent (window 1), max over a history window, current tensor
+ *    scaling (window 0 here).
+ *  - MX block scaling ("what actually breaks low precision training", "What
+ *    the measurements said"): one shared power of two per 32 values from the
+ *    OCP formula floor(log2(block amax)) - emax_elem; one extra bit of
+ *    exponent headroom as an option.
+ *
+ * Semantics fixed by this library where the pages are silent:
+ *  - Rounding: round to nearest, ties to even, on the format's grid; a
+ *    magnitude that rounds past the largest finite value saturates to
+ *    sign|max and counts as clipped (E4M3: |v| > 464; E5M2: |v| >= 61440).
+ *    +-Inf inputs saturate and count as clipped.  NaN -> sign|0x7F, not
+ *    clipped.  Zero and values that round to zero keep their sign.
+ *  - amax: max |x| with NaN > Inf > finite; any NaN gives the canonical NaN.
+ *  - Scale exponent e (scale = 2^e, scale_inv = 2^-e) is clamped to
+ *    [-126, 126].  A zero or non-finite window maximum keeps the previous e
+ *    (0 if none).  Hysteresis h: an upward move of 1..h binades keeps the
+ *    previous e; downward moves are immediate.
+ *  - The window holds the amaxes of the previous `window` casts of the
+ *    handle; the current amax enters it after the cast.  An empty window
+ *    (first cast, or window 0) uses current scaling: amax of this tensor
+ *    first, then the cast (two reads of x).
+ *  - MX: E clamped to [-127, 127]; an all-zero block gets E = -127 (byte
+ *    0x00); a block holding NaN or Inf gets E8M0 0xFF and every element byte
+ *    sign|0x7F.
+ *
+ * Conventions for every call:
+ *  - Return value: FP8Q_OK (0) or a negative FP8Q_E* status.  Nothing
+ *    throws.  fp8q_strerror() names a status; fp8q_last_cuda_error() gives
+ *    the text of the last CUDA error seen by the calling thread.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls taking a stream only enqueue work and return; outputs
+ *    are device memory, valid once the stream reaches that point.
+ *  - Tensors (x, q, e8m0, outputs) are device pointers owned by the caller;
+ *    the library never frees or retains them.  x and q must be 16-byte
+ *    aligned (else FP8Q_EALIGN).  x is read as a contiguous 1-D array of n
+ *    elements; q receives n bytes in the same order.
+ *  - A handle belongs to the device that was current at fp8q_create and must
+ *    be used with that device current (else FP8Q_EDEVICE).  A handle keeps
+ *    state across calls: do not use one handle from two streams at once.
+ *  - The library has no CPU path: without a usable GPU every compute call
+ *    returns FP8Q_ECUDA.
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FP8Q_API __attribute__((visibility("default")))
+#else
+#define FP8Q_API
+#endif
+
+/* 8-bit target formats */
+enum { FP8Q_E4M3 = 0, FP8Q_E5M2 = 1 };
+/* input element types */
+enum { FP8Q_F32 = 0, FP8Q_BF16 = 1 };
+/* status codes */
+enum {
+  FP8Q_OK = 0,
+  FP8Q_EINVAL = -1,   /* bad argument value (size, window, null pointer, ...) */
+  FP8Q_EALIGN = -2,   /* x or q not 16-byte aligned                         */
+  FP8Q_EDTYPE = -3,   /* unknown dtype or format                            */
+  FP8Q_ECUDA = -4,    /* a CUDA call failed; see fp8q_last_cuda_error()     */
+  FP8Q_EHANDLE = -5,  /* null or destroyed handle                           */
+  FP8Q_ENOMEM = -6,   /* device or host allocation failed                   */
+  FP8Q_EDEVICE = -7   /* handle used with another device current            */
+};
+
+/* Largest history window a handle may keep. */
+#define FP8Q_MAX_WINDOW 256
+/* "No previous exponent" in fp8q_scale_state / fp8q_set_history. */
+#define FP8Q_NO_EXP (-2147483647 - 1)
+
+typedef struct fp8q_state* fp8q_handle;
+
+/* Create the scaling state of one tensor ("Practice c06/E3" worked solution:
+ * per-tensor statistic, window, margin, hysteresis).
+ *   format      FP8Q_E4M3 or FP8Q_E5M2
+ *   window      0 (current scaling every call) .. FP8Q_MAX_WINDOW
+ *   margin_bits >= 0 and <= 16: the scale keeps amax <= fmax / 2^margin
+ *   hysteresis_bits >= 0 and <= 16 (0 = off)
+ * Allocates the state in device memory of the current device (cudaMalloc).
+ * *out receives the handle; FP8Q_ENOMEM / FP8Q_ECUDA on failure. */
+FP8Q_API int fp8q_create(int format, int window, int margin_bits, int hysteresis_bits,
+                         fp8q_handle* out);
+
+/* Free a handle's device and host state.  Waits for the handle's last cast.
+ * NULL is accepted (returns FP8Q_OK). */
+FP8Q_API int fp8q_destroy(fp8q_handle h);
+
+/* Fused scaled cast of one tensor (steps: amax reduction, scale from the
+ * window, saturating RNE cast with clipped count, cross-CTA finish).
+ *   x       device, n elements of `dtype` (FP8Q_F32 or FP8Q_BF16), 16-B aligned
+ *   n       >= 0 elements (any n; n = 0 records amax 0)
+ *   q       device, n bytes out (the handle's format), 16-B aligned
+ *   d_scale_inv, d_amax  device float out (scale_inv = 2^-e; amax of x), or NULL
+ *   d_clipped            device uint64 out (clipped count), or NULL
+ * One launch with a non-empty window (each element read once); two launches
+ * for current scaling of a tensor larger than one CTA chunk. */
+FP8Q_API int fp8q_cast(fp8q_handle h, const void* x, int dtype, int64_t n, uint8_t* q,
+                       float* d_scale_inv, float* d_amax, unsigned long long* d_clipped,
+                       void* stream);
+
+/* Grouped version of fp8q_cast over `count` tensors in one launch (plus one
+ * amax pre-pass launch if any tensor needs current scaling).  hs, xs,
+ * dtypes, ns, qs are HOST arrays of length count (xs/qs hold device
+ * pointers); the handles must be distinct.  d_scale_inv, d_amax, d_clipped
+ * are DEVICE arrays of length count (or NULL).  Work is split into equal
+ * 32 KiB input chunks over all tensors; each tensor keeps its own state.
+ * count > 0; groups above 512 tensors are split into several launches. */
+FP8Q_API int fp8q_cast_multi(const fp8q_handle* hs, const void* const* xs, const int* dtypes,
+                             const int64_t* ns, uint8_t* const* qs, float* d_scale_inv,
+                             float* d_amax, unsigned long long* d_clipped, int count,
+                             void* stream);
+
+/* MX block-scaled cast ("what actually breaks low precision training", "What
+ * the measurements said"): x is a row-major [rows, cols] tensor; each 32
+ * consecutive elements of a row share E = floor(log2(block amax)) -
+ * emax_elem + headroom_bits (emax_elem 8 for E4M3, 15 for E5M2).
+ *   cols          > 0 and a multiple of 32 (else FP8Q_EINVAL)
+ *   headroom_bits 0 (OCP rule) .. 4
+ *   q             device [rows, cols] bytes; e8m0: device [rows, cols/32] bytes (E+127)
+ *   d_clipped     device uint64 out (clipped elements), or NULL
+ * One kernel launch (plus a memset of d_clipped). */
+FP8Q_API int mx_cast(const void* x, int dtype, int64_t rows, int64_t cols, int format,
+                     int headroom_bits, uint8_t* q, uint8_t* e8m0,
+                     unsigned long long* d_clipped, void* stream);
+
+/* Read a handle's amax history (oldest first) to host memory.  Blocks until
+ * the handle's last cast has finished.  capacity must be >= the window;
+ * *n_valid receives the number of entries written. */
+FP8Q_API int fp8q_amax_history(fp8q_handle h, float* host_out, int capacity, int* n_valid);
+
+/* Read the exponent chosen by the last cast (FP8Q_NO_EXP if none yet) and
+ * the number of casts done.  Blocks like fp8q_amax_history.  Either
+ * pointer may be NULL. */
+FP8Q_API int fp8q_scale_state(fp8q_handle h, int* prev_exp, long long* steps);
+
+/* Restore a handle's state (resume from a checkpoint): n (<= window) amax
+ * values, oldest first, and the previous exponent (FP8Q_NO_EXP for none).
+ * Blocks until the handle's last cast has finished. */
+FP8Q_API int fp8q_set_history(fp8q_handle h, const float* host_in, int n, int prev_exp);
+
+/* Clear a handle's history and previous exponent (as after fp8q_create). */
+FP8Q_API int fp8q_reset(fp8q_handle h);
+
+/* Dequantised-error statistics of a per-tensor cast, over the elements whose
+ * input is finite ("what actually breaks low precision training": error size
+ * and bias measured separately).  deq = decode(q) * (*d_scale_inv).
+ *   d_out  device double[3] out: mean squared error, mean error (bias), count
+ * Sums are fp64, reduced in a fixed order (deterministic for a given GPU).
+ * Uses stream-ordered temporary device memory (cudaMallocAsync). */
+FP8Q_API int fp8q_error_stats(const void* x, int dtype, int64_t n, const uint8_t* q, int format,
+                              const float* d_scale_inv, double* d_out, void* stream);
+
+/* Same for an MX cast: deq = decode(q) * 2^E of its block; blocks whose
+ * E8M0 byte is 0xFF (NaN) are skipped. */
+FP8Q_API int mx_error_stats(const void* x, int dtype, int64_t rows, int64_t cols,
+                            const uint8_t* q, const uint8_t* e8m0, int format, double* d_out,
+                            void* stream);
+
+/* Name of a status code (static string). */
+FP8Q_API const char* fp8q_strerror(int code);
+
+/* Text of the last CUDA error seen by the calling thread ("" if none). */
+FP8Q_API const char* fp8q_last_cuda_error(void);
+
+/* Number of kernels this library has launched in this process. */
+FP8Q_API long long fp8q_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H */

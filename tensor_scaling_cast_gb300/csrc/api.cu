@@ -1,0 +1,376 @@
+// C ABI of libfp8q: argument checks, handle lifecycle, launch planning.
+// Every entry point returns a status; nothing throws across the ABI.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "fp8q.h"
+#include "fp8q_internal.cuh"
+
+namespace fp8q {
+
+static std::atomic<long long> g_launches{0};
+static thread_local char g_cuda_err[256] = "";
+
+static int fail_cuda(cudaError_t e) {
+  std::snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return FP8Q_ECUDA;
+}
+
+int device_of_current() {
+  int d = 0;
+  cudaGetDevice(&d);
+  return d;
+}
+
+int sm_count(int device) {
+  static std::mutex mu;
+  static int cache[128] = {0};
+  if (device < 0 || device >= 128) return 1;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[device] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || v < 1) v = 1;
+    cache[device] = v;
+  }
+  return cache[device];
+}
+
+}  // namespace fp8q
+
+using namespace fp8q;
+
+static const uint32_t kMagic = 0xF8A5C0DEu;
+
+struct fp8q_state {
+  uint32_t magic;
+  int format, window, margin, hyst;
+  int device;
+  DevState* dev;
+  int host_count;           // valid history entries, mirrored on the host
+  cudaEvent_t last;         // recorded after each cast on its stream
+  bool has_last;
+};
+
+static bool handle_ok(fp8q_handle h) { return h != nullptr && h->magic == kMagic; }
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool dtype_ok(int d) { return d == FP8Q_F32 || d == FP8Q_BF16; }
+static bool format_ok(int f) { return f == FP8Q_E4M3 || f == FP8Q_E5M2; }
+
+static int check_device(fp8q_handle h) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return d == h->device ? FP8Q_OK : FP8Q_EDEVICE;
+}
+
+// Wait for the handle's last cast (before a host read or write of its state).
+static int wait_last(fp8q_handle h) {
+  if (!h->has_last) return FP8Q_OK;
+  cudaError_t e = cudaEventSynchronize(h->last);
+  return e == cudaSuccess ? FP8Q_OK : fail_cuda(e);
+}
+
+static int record_last(fp8q_handle h, cudaStream_t s) {
+  cudaError_t e = cudaEventRecord(h->last, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  h->has_last = true;
+  return FP8Q_OK;
+}
+
+extern "C" {
+
+FP8Q_API const char* fp8q_strerror(int code) {
+  switch (code) {
+    case FP8Q_OK: return "ok";
+    case FP8Q_EINVAL: return "invalid argument";
+    case FP8Q_EALIGN: return "pointer not 16-byte aligned";
+    case FP8Q_EDTYPE: return "unsupported dtype or format";
+    case FP8Q_ECUDA: return "CUDA error";
+    case FP8Q_EHANDLE: return "invalid handle";
+    case FP8Q_ENOMEM: return "out of memory";
+    case FP8Q_EDEVICE: return "handle used on another device";
+    default: return "unknown status";
+  }
+}
+
+FP8Q_API const char* fp8q_last_cuda_error(void) { return g_cuda_err; }
+
+FP8Q_API long long fp8q_launch_count(void) { return g_launches.load(); }
+
+FP8Q_API int fp8q_create(int format, int window, int margin_bits, int hysteresis_bits,
+                         fp8q_handle* out) {
+  if (!out) return FP8Q_EINVAL;
+  *out = nullptr;
+  if (!format_ok(format)) return FP8Q_EDTYPE;
+  if (window < 0 || window > FP8Q_MAX_WINDOW || margin_bits < 0 || margin_bits > 16 ||
+      hysteresis_bits < 0 || hysteresis_bits > 16)
+    return FP8Q_EINVAL;
+  fp8q_state* h = new (std::nothrow) fp8q_state();
+  if (!h) return FP8Q_ENOMEM;
+  h->format = format;
+  h->window = window;
+  h->margin = margin_bits;
+  h->hyst = hysteresis_bits;
+  h->host_count = 0;
+  h->has_last = false;
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e != cudaSuccess) { delete h; return fail_cuda(e); }
+  e = cudaMalloc(reinterpret_cast<void**>(&h->dev), sizeof(DevState));
+  if (e != cudaSuccess) { delete h; return e == cudaErrorMemoryAllocation ? FP8Q_ENOMEM : fail_cuda(e); }
+  DevState init;
+  std::memset(&init, 0, sizeof init);
+  init.format = format;
+  init.window = window;
+  init.margin = margin_bits;
+  init.hyst = hysteresis_bits;
+  e = cudaMemcpy(h->dev, &init, sizeof init, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->last, cudaEventDisableTiming);
+  if (e != cudaSuccess) { cudaFree(h->dev); delete h; return fail_cuda(e); }
+  h->magic = kMagic;
+  *out = h;
+  return FP8Q_OK;
+}
+
+FP8Q_API int fp8q_destroy(fp8q_handle h) {
+  if (h == nullptr) return FP8Q_OK;
+  if (!handle_ok(h)) return FP8Q_EHANDLE;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaSetDevice(h->device);
+  if (h->has_last) cudaEventSynchronize(h->last);
+  cudaEventDestroy(h->last);
+  cudaError_t e = cudaFree(h->dev);
+  cudaSetDevice(dev);
+  h->magic = 0;
+  delete h;
+  return e == cudaSuccess ? FP8Q_OK : fail_cuda(e);
+}
+
+// Build the descriptors of a group, launch the current-scaling pre-pass for
+// the tensors that need it, then the fused cast.
+static int plan_and_launch(const fp8q_handle* hs, const void* const* xs, const int* dtypes,
+                           const int64_t* ns, uint8_t* const* qs, float* d_scale_inv,
+                           float* d_amax, unsigned long long* d_clipped, int count,
+                           cudaStream_t s) {
+  for (int base = 0; base < count; base += kMaxGroup) {
+    const int m = std::min(kMaxGroup, count - base);
+    std::vector<TensorDesc> all(m), pre;
+    long long chunks = 0, pre_chunks = 0;
+    for (int i = 0; i < m; ++i) {
+      const fp8q_handle h = hs[base + i];
+      const int dt = dtypes[base + i];
+      const int64_t n = ns[base + i];
+      const int64_t ce = chunk_elems(dt);
+      const long long nch = std::max<long long>(1, (n + ce - 1) / ce);
+      int mode = kDelayed;
+      if (h->window == 0 || h->host_count == 0) mode = (n <= ce) ? kCurrentLocal : kCurrentPre;
+      TensorDesc d;
+      d.x = xs[base + i];
+      d.q = qs[base + i];
+      d.n = n;
+      d.st = h->dev;
+      d.chunk_begin = (int32_t)chunks;
+      d.flags = (dt == FP8Q_BF16 ? 1 : 0) | (h->format == FP8Q_E5M2 ? 2 : 0) | (mode << 2);
+      all[i] = d;
+      chunks += nch;
+      if (mode == kCurrentPre) {
+        TensorDesc p = d;
+        p.chunk_begin = (int32_t)pre_chunks;
+        pre.push_back(p);
+        pre_chunks += nch;
+      }
+    }
+    if (chunks > 0x7FFFFFFFll) return FP8Q_EINVAL;
+    int launches = 0;
+    GroupHeader gh;
+    std::memset(&gh, 0, sizeof gh);
+    if (!pre.empty()) {
+      gh.total_chunks = (int32_t)pre_chunks;
+      cudaError_t e = launch_amax_group(gh, pre.data(), (int)pre.size(), s, &launches);
+      g_launches += launches;
+      if (e != cudaSuccess) return fail_cuda(e);
+      launches = 0;
+    }
+    gh.scale_inv = d_scale_inv;
+    gh.amax = d_amax;
+    gh.clipped = d_clipped;
+    gh.total_chunks = (int32_t)chunks;
+    gh.out_offset = base;
+    cudaError_t e = launch_cast_group(gh, all.data(), m, s, &launches);
+    g_launches += launches;
+    if (e != cudaSuccess) return fail_cuda(e);
+    for (int i = 0; i < m; ++i) {
+      fp8q_handle h = hs[base + i];
+      if (h->window > 0 && h->host_count < h->window) h->host_count++;
+      int st = record_last(h, s);
+      if (st != FP8Q_OK) return st;
+    }
+  }
+  return FP8Q_OK;
+}
+
+static int check_tensor(fp8q_handle h, const void* x, int dtype, int64_t n, const uint8_t* q) {
+  if (!handle_ok(h)) return FP8Q_EHANDLE;
+  if (!dtype_ok(dtype)) return FP8Q_EDTYPE;
+  if (n < 0 || n > (int64_t(1) << 46)) return FP8Q_EINVAL;
+  if (n > 0 && (x == nullptr || q == nullptr)) return FP8Q_EINVAL;
+  if (!aligned16(x) || !aligned16(q)) return FP8Q_EALIGN;
+  return FP8Q_OK;
+}
+
+FP8Q_API int fp8q_cast(fp8q_handle h, const void* x, int dtype, int64_t n, uint8_t* q,
+                       float* d_scale_inv, float* d_amax, unsigned long long* d_clipped,
+                       void* stream) {
+  int st = check_tensor(h, x, dtype, n, q);
+  if (st != FP8Q_OK) return st;
+  st = check_device(h);
+  if (st != FP8Q_OK) return st;
+  return plan_and_launch(&h, &x, &dtype, &n, &q, d_scale_inv, d_amax, d_clipped, 1,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+FP8Q_API int fp8q_cast_multi(const fp8q_handle* hs, const void* const* xs, const int* dtypes,
+                             const int64_t* ns, uint8_t* const* qs, float* d_scale_inv,
+                             float* d_amax, unsigned long long* d_clipped, int count,
+                             void* stream) {
+  if (count <= 0 || !hs || !xs || !dtypes || !ns || !qs) return FP8Q_EINVAL;
+  for (int i = 0; i < count; ++i) {
+    int st = check_tensor(hs[i], xs[i], dtypes[i], ns[i], qs[i]);
+    if (st != FP8Q_OK) return st;
+    st = check_device(hs[i]);
+    if (st != FP8Q_OK) return st;
+  }
+  std::vector<fp8q_handle> sorted(hs, hs + count);
+  std::sort(sorted.begin(), sorted.end());
+  if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end()) return FP8Q_EINVAL;
+  return plan_and_launch(hs, xs, dtypes, ns, qs, d_scale_inv, d_amax, d_clipped, count,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+FP8Q_API int mx_cast(const void* x, int dtype, int64_t rows, int64_t cols, int format,
+                     int headroom_bits, uint8_t* q, uint8_t* e8m0,
+                     unsigned long long* d_clipped, void* stream) {
+  if (!dtype_ok(dtype) || !format_ok(format)) return FP8Q_EDTYPE;
+  if (rows < 0 || cols <= 0 || cols % 32 != 0 || headroom_bits < 0 || headroom_bits > 4)
+    return FP8Q_EINVAL;
+  if (rows > 0 && cols > (int64_t(1) << 46) / rows) return FP8Q_EINVAL;
+  const int64_t n = rows * cols;
+  if (n > 0 && (!x || !q || !e8m0)) return FP8Q_EINVAL;
+  if (!aligned16(x) || !aligned16(q)) return FP8Q_EALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (d_clipped) {
+    cudaError_t e = cudaMemsetAsync(d_clipped, 0, sizeof(unsigned long long), s);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  if (n == 0) return FP8Q_OK;
+  int launches = 0;
+  cudaError_t e = launch_mx(x, dtype, n, format, headroom_bits, q, e8m0, d_clipped, s, &launches);
+  g_launches += launches;
+  return e == cudaSuccess ? FP8Q_OK : fail_cuda(e);
+}
+
+FP8Q_API int fp8q_amax_history(fp8q_handle h, float* host_out, int capacity, int* n_valid) {
+  if (!handle_ok(h)) return FP8Q_EHANDLE;
+  if (!n_valid || (capacity > 0 && !host_out) || capacity < h->window) return FP8Q_EINVAL;
+  int st = check_device(h);
+  if (st == FP8Q_OK) st = wait_last(h);
+  if (st != FP8Q_OK) return st;
+  DevState d;
+  cudaError_t e = cudaMemcpy(&d, h->dev, sizeof d, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e);
+  const int cnt = d.count;
+  // oldest first: with a full ring the oldest entry sits at head
+  for (int i = 0; i < cnt; ++i) {
+    const int slot = (cnt < h->window) ? i : (d.head + i) % h->window;
+    std::memcpy(&host_out[i], &d.ring[slot], 4);
+  }
+  *n_valid = cnt;
+  return FP8Q_OK;
+}
+
+FP8Q_API int fp8q_scale_state(fp8q_handle h, int* prev_exp, long long* steps) {
+  if (!handle_ok(h)) return FP8Q_EHANDLE;
+  int st = check_device(h);
+  if (st == FP8Q_OK) st = wait_last(h);
+  if (st != FP8Q_OK) return st;
+  DevState d;
+  cudaError_t e = cudaMemcpy(&d, h->dev, sizeof d, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (prev_exp) *prev_exp = d.has_prev ? d.prev_e : FP8Q_NO_EXP;
+  if (steps) *steps = d.steps;
+  return FP8Q_OK;
+}
+
+static int write_state(fp8q_handle h, const float* host_in, int n, int prev_exp, long long steps) {
+  int st = check_device(h);
+  if (st == FP8Q_OK) st = wait_last(h);
+  if (st != FP8Q_OK) return st;
+  DevState d;
+  std::memset(&d, 0, sizeof d);
+  d.format = h->format;
+  d.window = h->window;
+  d.margin = h->margin;
+  d.hyst = h->hyst;
+  for (int i = 0; i < n; ++i) {
+    uint32_t b;
+    std::memcpy(&b, &host_in[i], 4);
+    b &= 0x7FFFFFFFu;
+    d.ring[i] = b > 0x7F800000u ? 0x7FC00000u : b;
+  }
+  d.count = n;
+  d.head = (h->window > 0) ? n % h->window : 0;
+  d.has_prev = prev_exp != FP8Q_NO_EXP;
+  d.prev_e = d.has_prev ? prev_exp : 0;
+  d.steps = steps;
+  cudaError_t e = cudaMemcpy(h->dev, &d, sizeof d, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fail_cuda(e);
+  h->host_count = n;
+  return FP8Q_OK;
+}
+
+FP8Q_API int fp8q_set_history(fp8q_handle h, const float* host_in, int n, int prev_exp) {
+  if (!handle_ok(h)) return FP8Q_EHANDLE;
+  if (n < 0 || n > h->window || (n > 0 && !host_in)) return FP8Q_EINVAL;
+  if (prev_exp != FP8Q_NO_EXP && (prev_exp < -126 || prev_exp > 126)) return FP8Q_EINVAL;
+  return write_state(h, host_in, n, prev_exp, 0);
+}
+
+FP8Q_API int fp8q_reset(fp8q_handle h) {
+  if (!handle_ok(h)) return FP8Q_EHANDLE;
+  return write_state(h, nullptr, 0, FP8Q_NO_EXP, 0);
+}
+
+FP8Q_API int fp8q_error_stats(const void* x, int dtype, int64_t n, const uint8_t* q, int format,
+                              const float* d_scale_inv, double* d_out, void* stream) {
+  if (!dtype_ok(dtype) || !format_ok(format)) return FP8Q_EDTYPE;
+  if (n < 0 || !d_out || !d_scale_inv || (n > 0 && (!x || !q))) return FP8Q_EINVAL;
+  int launches = 0;
+  cudaError_t e = launch_stats(x, dtype, n, q, format, d_scale_inv, nullptr, d_out,
+                               reinterpret_cast<cudaStream_t>(stream), &launches);
+  g_launches += launches;
+  return e == cudaSuccess ? FP8Q_OK : fail_cuda(e);
+}
+
+FP8Q_API int mx_error_stats(const void* x, int dtype, int64_t rows, int64_t cols,
+                            const uint8_t* q, const uint8_t* e8m0, int format, double* d_out,
+                            void* stream) {
+  if (!dtype_ok(dtype) || !format_ok(format)) return FP8Q_EDTYPE;
+  if (rows < 0 || cols <= 0 || cols % 32 != 0 || !d_out) return FP8Q_EINVAL;
+  const int64_t n = rows * cols;
+  if (n > 0 && (!x || !q || !e8m0)) return FP8Q_EINVAL;
+  int launches = 0;
+  cudaError_t e = launch_stats(x, dtype, n, q, format, nullptr, e8m0, d_out,
+                               reinterpret_cast<cudaStream_t>(stream), &launches);
+  g_launches += launches;
+  return e == cudaSuccess ? FP8Q_OK : fail_cuda(e);
+}
+
+}  // extern "C"

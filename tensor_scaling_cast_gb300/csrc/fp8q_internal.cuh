@@ -1,0 +1,79 @@
+// Internal definitions shared by the libfp8q translation units (device
+// state layout, launch descriptors, small device helpers).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fp8q.h"
+
+namespace fp8q {
+
+constexpr int kThreads = 256;                 // threads per CTA (8 warps)
+constexpr int kUnroll = 8;                    // 16-byte loads in flight per thread
+constexpr int kChunkBytes = kThreads * kUnroll * 16;   // 32 KiB of input per chunk
+constexpr int kMaxGroup = 512;                // tensors per grouped launch
+
+// Device-resident scaling state of one tensor (one per handle).
+struct __align__(256) DevState {
+  uint32_t ring[FP8Q_MAX_WINDOW];   // amax fp32 bits of past casts (ring order)
+  uint32_t amax_acc;                // running max of |x| bits, this cast
+  uint32_t pre_amax;                // current-scaling pre-pass result
+  unsigned long long clip_acc;      // clipped elements, this cast
+  uint32_t ticket;                  // chunks finished, this cast
+  int32_t count;                    // valid ring entries (<= window)
+  int32_t head;                     // next ring slot
+  int32_t prev_e;                   // exponent of the last cast
+  int32_t has_prev;
+  int32_t format, window, margin, hyst;
+  long long steps;
+};
+
+enum Mode : int { kDelayed = 0, kCurrentPre = 1, kCurrentLocal = 2 };
+
+// One tensor of a grouped launch (40 bytes; kept in the kernel's
+// parameter space, so a 512-tensor group needs no device-side table).
+struct TensorDesc {
+  const void* x;
+  uint8_t* q;
+  int64_t n;
+  DevState* st;
+  int32_t chunk_begin;              // first chunk of this tensor in the group
+  int32_t flags;                    // bit0 bf16, bit1 E5M2, bits2-3 Mode
+};
+
+struct GroupHeader {
+  float* scale_inv;                 // [out_offset + t] outputs, nullable
+  float* amax;
+  unsigned long long* clipped;
+  int32_t count;
+  int32_t total_chunks;
+  int32_t out_offset;
+  int32_t pad;
+};
+
+template <int MAXT>
+struct GroupParams {
+  GroupHeader h;
+  TensorDesc d[MAXT];
+};
+
+inline int chunk_elems(int dtype) { return kChunkBytes / (dtype == FP8Q_BF16 ? 2 : 4); }
+
+// ---- launches (defined in cast.cu / mx.cu / stats.cu) ----------------------
+// Each returns a cudaError_t from the launch.
+cudaError_t launch_cast_group(const GroupHeader& h, const TensorDesc* d, int count,
+                              cudaStream_t s, int* launches);
+cudaError_t launch_amax_group(const GroupHeader& h, const TensorDesc* d, int count,
+                              cudaStream_t s, int* launches);
+cudaError_t launch_mx(const void* x, int dtype, int64_t nelem, int format, int headroom,
+                      uint8_t* q, uint8_t* e8m0, unsigned long long* clipped, cudaStream_t s,
+                      int* launches);
+cudaError_t launch_stats(const void* x, int dtype, int64_t n, const uint8_t* q, int format,
+                         const float* scale_inv, const uint8_t* e8m0, double* out,
+                         cudaStream_t s, int* launches);
+
+int sm_count(int device);
+int device_of_current();
+
+}  // namespace fp8q

@@ -1,0 +1,225 @@
+"""Thin Python binding of libfp8q's C ABI (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of the method: it turns torch tensors into device pointers, the
+current torch stream into a ``cudaStream_t`` and a non-zero status into an
+exception.  There is no CPU path: if ``libfp8q.so`` is missing or no GPU is
+usable the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfp8q.so")
+
+E4M3, E5M2 = 0, 1
+F32, BF16 = 0, 1
+NO_EXP = -(2 ** 31)
+MAX_WINDOW = 256
+
+_STATUS = {0: "FP8Q_OK", -1: "FP8Q_EINVAL", -2: "FP8Q_EALIGN", -3: "FP8Q_EDTYPE", -4: "FP8Q_ECUDA",
+           -5: "FP8Q_EHANDLE", -6: "FP8Q_ENOMEM", -7: "FP8Q_EDEVICE"}
+
+
+class Fp8qError(RuntimeError):
+    def __init__(self, status: int, what: str, detail: str = ""):
+        self.status = status
+        msg = f"{what} failed: {_STATUS.get(status, status)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libfp8q.so (built by ``__graft_entry__.build()`` or
+    ``tensor_scaling_cast_gb300.build``).  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built; run tensor_scaling_cast_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    p, i, i64, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    L.fp8q_create.argtypes = [i, i, i, i, ctypes.POINTER(p)]
+    L.fp8q_destroy.argtypes = [p]
+    L.fp8q_cast.argtypes = [p, p, i, i64, p, p, p, p, p]
+    L.fp8q_cast_multi.argtypes = [p, p, p, p, p, p, p, p, i, p]
+    L.mx_cast.argtypes = [p, i, i64, i64, i, i, p, p, p, p]
+    L.fp8q_amax_history.argtypes = [p, ctypes.POINTER(f), i, ctypes.POINTER(i)]
+    L.fp8q_scale_state.argtypes = [p, ctypes.POINTER(i), ctypes.POINTER(ctypes.c_longlong)]
+    L.fp8q_set_history.argtypes = [p, ctypes.POINTER(f), i, i]
+    L.fp8q_reset.argtypes = [p]
+    L.fp8q_error_stats.argtypes = [p, i, i64, p, i, p, p, p]
+    L.mx_error_stats.argtypes = [p, i, i64, i64, p, p, i, p, p]
+    L.fp8q_strerror.argtypes = [i]
+    L.fp8q_strerror.restype = ctypes.c_char_p
+    L.fp8q_last_cuda_error.restype = ctypes.c_char_p
+    L.fp8q_launch_count.restype = ctypes.c_longlong
+    for name in ("fp8q_create", "fp8q_destroy", "fp8q_cast", "fp8q_cast_multi", "mx_cast",
+                 "fp8q_amax_history", "fp8q_scale_state", "fp8q_set_history", "fp8q_reset",
+                 "fp8q_error_stats", "mx_error_stats"):
+        getattr(L, name).restype = i
+    _lib = L
+    return L
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        detail = ""
+        if status == -4:
+            detail = load().fp8q_last_cuda_error().decode()
+        raise Fp8qError(status, what, detail)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported input dtype {t.dtype}: bf16 or fp32")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def launch_count() -> int:
+    return int(load().fp8q_launch_count())
+
+
+# ---- handles ---------------------------------------------------------------
+
+def fp8q_create(fmt: int, window: int, margin: int = 0, hysteresis: int = 0) -> int:
+    h = ctypes.c_void_p()
+    _check(load().fp8q_create(fmt, window, margin, hysteresis, ctypes.byref(h)), "fp8q_create")
+    return h.value
+
+
+def fp8q_destroy(h: int):
+    _check(load().fp8q_destroy(ctypes.c_void_p(h)), "fp8q_destroy")
+
+
+def fp8q_cast(h: int, x: torch.Tensor, q: torch.Tensor, scale_inv=None, amax=None, clipped=None,
+              stream=None):
+    """x: contiguous bf16/fp32 CUDA tensor; q: uint8 CUDA tensor of x.numel()
+    bytes; scale_inv / amax: float32 CUDA scalars; clipped: int64 CUDA scalar
+    (read as uint64)."""
+    _check(load().fp8q_cast(ctypes.c_void_p(h), _ptr(x), _dtype(x), x.numel(), _ptr(q),
+                            _ptr(scale_inv), _ptr(amax), _ptr(clipped), _stream(stream)),
+           "fp8q_cast")
+
+
+def fp8q_cast_multi(hs, xs, qs, scale_inv=None, amax=None, clipped=None, stream=None):
+    """hs: handles; xs / qs: lists of CUDA tensors; scale_inv / amax: float32
+    CUDA tensors [count]; clipped: int64 CUDA tensor [count]."""
+    n = len(hs)
+    H = (ctypes.c_void_p * n)(*hs)
+    X = (ctypes.c_void_p * n)(*[x.data_ptr() for x in xs])
+    Q = (ctypes.c_void_p * n)(*[q.data_ptr() for q in qs])
+    D = (ctypes.c_int * n)(*[_dtype(x) for x in xs])
+    N = (ctypes.c_int64 * n)(*[x.numel() for x in xs])
+    _check(load().fp8q_cast_multi(H, X, D, N, Q, _ptr(scale_inv), _ptr(amax), _ptr(clipped), n,
+                                  _stream(stream)), "fp8q_cast_multi")
+
+
+def mx_cast(x: torch.Tensor, fmt: int, headroom: int, q: torch.Tensor, e8m0: torch.Tensor,
+            clipped=None, stream=None):
+    rows, cols = x.shape
+    _check(load().mx_cast(_ptr(x), _dtype(x), rows, cols, fmt, headroom, _ptr(q), _ptr(e8m0),
+                          _ptr(clipped), _stream(stream)), "mx_cast")
+
+
+def fp8q_amax_history(h: int, capacity: int = MAX_WINDOW) -> list[float]:
+    buf = (ctypes.c_float * max(1, capacity))()
+    nv = ctypes.c_int()
+    _check(load().fp8q_amax_history(ctypes.c_void_p(h), buf, capacity, ctypes.byref(nv)),
+           "fp8q_amax_history")
+    return [buf[i] for i in range(nv.value)]
+
+
+def fp8q_scale_state(h: int):
+    """(previous exponent or None, number of casts)."""
+    e = ctypes.c_int()
+    st = ctypes.c_longlong()
+    _check(load().fp8q_scale_state(ctypes.c_void_p(h), ctypes.byref(e), ctypes.byref(st)),
+           "fp8q_scale_state")
+    return (None if e.value == NO_EXP else e.value), st.value
+
+
+def fp8q_set_history(h: int, values, prev_exp=None):
+    buf = (ctypes.c_float * max(1, len(values)))(*values)
+    _check(load().fp8q_set_history(ctypes.c_void_p(h), buf, len(values),
+                                   NO_EXP if prev_exp is None else int(prev_exp)),
+           "fp8q_set_history")
+
+
+def fp8q_reset(h: int):
+    _check(load().fp8q_reset(ctypes.c_void_p(h)), "fp8q_reset")
+
+
+def fp8q_error_stats(x: torch.Tensor, q: torch.Tensor, fmt: int, scale_inv: torch.Tensor,
+                     out: torch.Tensor, stream=None):
+    _check(load().fp8q_error_stats(_ptr(x), _dtype(x), x.numel(), _ptr(q), fmt, _ptr(scale_inv),
+                                   _ptr(out), _stream(stream)), "fp8q_error_stats")
+
+
+def mx_error_stats(x: torch.Tensor, q: torch.Tensor, e8m0: torch.Tensor, fmt: int,
+                   out: torch.Tensor, stream=None):
+    rows, cols = x.shape
+    _check(load().mx_error_stats(_ptr(x), _dtype(x), rows, cols, _ptr(q), _ptr(e8m0), fmt,
+                                 _ptr(out), _stream(stream)), "mx_error_stats")
+
+
+# ---- convenience wrapper ---------------------------------------------------
+
+class ScaledCast:
+    """One tensor's scaling state on the GPU (owns an fp8q handle) with
+    output buffers allocated by torch."""
+
+    def __init__(self, fmt: int, window: int, margin: int = 0, hysteresis: int = 0):
+        self.fmt, self.window, self.margin, self.hysteresis = fmt, window, margin, hysteresis
+        self.handle = fp8q_create(fmt, window, margin, hysteresis)
+
+    def __call__(self, x: torch.Tensor, q: torch.Tensor | None = None, stream=None):
+        """Returns (q uint8, scale_inv f32[1], amax f32[1], clipped i64[1]) on x's device."""
+        dev = x.device
+        if q is None:
+            q = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+        outs = torch.empty(2, dtype=torch.float32, device=dev)
+        clipped = torch.empty(1, dtype=torch.int64, device=dev)
+        fp8q_cast(self.handle, x, q, outs[0:1], outs[1:2], clipped, stream)
+        return q, outs[0:1], outs[1:2], clipped
+
+    def history(self):
+        return fp8q_amax_history(self.handle, max(1, self.window))
+
+    def state(self):
+        return fp8q_scale_state(self.handle)
+
+    def set_history(self, values, prev_exp=None):
+        fp8q_set_history(self.handle, values, prev_exp)
+
+    def reset(self):
+        fp8q_reset(self.handle)
+
+    def close(self):
+        if self.handle:
+            fp8q_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,369 @@
+"""Parity of the sm_103a kernels (through the C ABI) with the CPU oracle.
+
+Bar: bit-exact for FP8 bytes, E8M0 bytes, amax, scale_inv and clipped counts;
+error statistics within 1e-6 relative.  Inputs come from the seeded
+generators; the oracle receives the same bytes copied to the host.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import coracle, policy
+from tensor_scaling_cast_gb300 import fp8q as F
+from tensor_scaling_cast_gb300 import synthetic
+
+pytestmark = pytest.mark.gpu
+
+NT = os.cpu_count() or 1
+EMAX = {0: 8, 1: 15}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA GPU is required for the gpu tests")
+    from tensor_scaling_cast_gb300 import build
+    build.build()
+    F.load()
+    torch.cuda.set_device(0)
+
+
+def host_bits(x: torch.Tensor) -> np.ndarray:
+    x = x.detach().contiguous().cpu()
+    if x.dtype == torch.bfloat16:
+        return x.view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    return x.view(torch.int32).numpy().view(np.uint32).reshape(-1)
+
+
+def f32bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int32).numpy().view(np.uint32).reshape(-1)
+
+
+def from_bits(bits: np.ndarray, dtype) -> torch.Tensor:
+    if dtype == torch.bfloat16:
+        return torch.from_numpy(bits.astype(np.uint16).view(np.int16).copy()).view(torch.bfloat16)
+    return torch.from_numpy(bits.astype(np.uint32).view(np.int32).copy()).view(torch.float32)
+
+
+def set_exponent(h: int, fmt: int, e: int):
+    """Plant a one-entry window whose maximum makes the rule choose e."""
+    F.fp8q_set_history(h, [float(2.0 ** (EMAX[fmt] - e))], None)
+
+
+# ---------------------------------------------------------------------------
+# the conversion itself, through the full kernel path
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_every_bf16_pattern_every_scale(fmt):
+    """All 65,536 bf16 bit patterns (zeros, subnormals, Inf, NaN included),
+    four copies so the launch spans several chunks, at exponents covering the
+    reachable range: bytes, amax, scale_inv and clipped count exact."""
+    bits = np.tile(np.arange(65536, dtype=np.uint32).astype(np.uint16), 4)
+    x = from_bits(bits, torch.bfloat16).cuda()
+    h = F.fp8q_create(fmt, 1, 0, 0)
+    q = torch.empty(x.numel(), dtype=torch.uint8, device="cuda")
+    out = torch.empty(2, dtype=torch.float32, device="cuda")
+    clipped = torch.empty(1, dtype=torch.int64, device="cuda")
+    lo = EMAX[fmt] - 127
+    for e in sorted(set(list(range(lo, 127, 7)) + [lo, lo + 1, -1, 0, 1, 125, 126])):
+        set_exponent(h, fmt, e)
+        F.fp8q_cast(h, x, q, out[0:1], out[1:2], clipped)
+        torch.cuda.synchronize()
+        q_o, a_o, c_o = coracle.cast(bits, fmt, e, NT)
+        got = q.cpu().numpy()
+        bad = np.nonzero(got != q_o)[0]
+        assert bad.size == 0, (e, [(hex(int(bits[i])), hex(int(got[i])), hex(int(q_o[i]))) for i in bad[:8]])
+        assert f32bits(out)[0] == np.float32(2.0 ** -e).view(np.uint32)
+        assert f32bits(out)[1] == a_o
+        assert int(clipped.item()) == c_o
+    F.fp8q_destroy(h)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_random_fp32_patterns(fmt):
+    rng = np.random.default_rng(5)
+    bits = rng.integers(0, 2 ** 32, size=(1 << 20) + 5, dtype=np.uint64).astype(np.uint32)
+    x = from_bits(bits, torch.float32).cuda()
+    h = F.fp8q_create(fmt, 1, 0, 0)
+    q = torch.empty(x.numel(), dtype=torch.uint8, device="cuda")
+    clipped = torch.empty(1, dtype=torch.int64, device="cuda")
+    for e in (EMAX[fmt] - 127, -60, -3, 0, 17, 90, 126):
+        set_exponent(h, fmt, e)
+        F.fp8q_cast(h, x, q, None, None, clipped)
+        torch.cuda.synchronize()
+        q_o, _, c_o = coracle.cast(bits, fmt, e, NT)
+        assert np.array_equal(q.cpu().numpy(), q_o), e
+        assert int(clipped.item()) == c_o
+    F.fp8q_destroy(h)
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+def run_steps(gpu_caster, orc_state, xs):
+    """Cast a sequence through one handle and the oracle; compare all."""
+    records = []
+    for t, x in enumerate(xs):
+        q, sinv, amax, clipped = gpu_caster(x)
+        torch.cuda.synchronize()
+        q_o, a_o, s_o, c_o, e_o = orc_state.step(host_bits(x), NT)
+        assert np.array_equal(q.cpu().numpy().reshape(-1), q_o.reshape(-1)), f"bytes differ at step {t}"
+        assert f32bits(amax)[0] == a_o, t
+        assert f32bits(sinv)[0] == s_o, t
+        assert int(clipped.item()) == c_o, t
+        records.append((e_o, c_o))
+    return records
+
+
+def test_current_scaling_4096_fp32():
+    x = synthetic.current_4096("cuda")
+    g = F.ScaledCast(F.E4M3, window=0, margin=0)
+    o = policy.ScalingState(0, window=0, margin=0)
+    recs = run_steps(g, o, [x, x * 3.0, x * 1e-3])
+    assert all(c == 0 for _, c in recs)             # current scaling never clips
+    g.close()
+
+
+@pytest.mark.parametrize("window,margin", [(1, 0), (16, 1)])
+def test_spike_sequence(window, margin):
+    """16 steps of bf16 4096x4096 with a x8 spike on 0.1% of step 9."""
+    g = F.ScaledCast(F.E4M3, window=window, margin=margin)
+    o = policy.ScalingState(0, window=window, margin=margin)
+    xs = (synthetic.spike_step(s, "cuda") for s in range(synthetic.SPIKE_STEPS))
+    recs = run_steps(g, o, xs)
+    clipped = [c for _, c in recs]
+    if window == 1:
+        assert clipped[synthetic.SPIKE_STEP] > 0
+    hist = g.history()
+    assert [np.float32(v).view(np.uint32) for v in hist] == o.hist
+    assert g.state() == (o.prev_e, 16)
+    g.close()
+
+
+def run_group_steps(fmts, windows, xs_steps, margin=0, hyst=0, check_every=True):
+    hs = [F.fp8q_create(f, w, margin, hyst) for f, w in zip(fmts, windows)]
+    orc = [policy.ScalingState(f, w, margin, hyst) for f, w in zip(fmts, windows)]
+    n = len(hs)
+    for t, xs in enumerate(xs_steps):
+        qs = [torch.empty(x.numel(), dtype=torch.uint8, device="cuda") for x in xs]
+        sinv = torch.empty(n, dtype=torch.float32, device="cuda")
+        amax = torch.empty(n, dtype=torch.float32, device="cuda")
+        clipped = torch.empty(n, dtype=torch.int64, device="cuda")
+        F.fp8q_cast_multi(hs, xs, qs, sinv, amax, clipped)
+        torch.cuda.synchronize()
+        sb, ab, cb = f32bits(sinv), f32bits(amax), clipped.cpu().numpy()
+        for i, x in enumerate(xs):
+            q_o, a_o, s_o, c_o, e_o = orc[i].step(host_bits(x), NT)
+            assert np.array_equal(qs[i].cpu().numpy(), q_o.reshape(-1)), (t, i)
+            assert ab[i] == a_o and sb[i] == s_o and int(cb[i]) == c_o, (t, i)
+        del qs
+    for h, o in zip(hs, orc):
+        assert F.fp8q_scale_state(h) == (o.prev_e, o.steps)
+        F.fp8q_destroy(h)
+
+
+def test_grad_group_reduced_sizes():
+    """64 gradient-like bf16 tensors (sides 64..512) -> E5M2, window 16, one
+    grouped launch per step, 4 steps (step 0 is current scaling)."""
+    steps = [synthetic.grad_group_step(s, "cuda", sides=(64, 128, 256, 512)) for s in range(4)]
+    run_group_steps([1] * 64, [16] * 64, steps)
+
+
+def test_grad_group_full_size():
+    """The full 64-tensor group (sides 1024..8192, ~9.4e8 elements per
+    step), 3 steps, every byte compared."""
+    hs_steps = (synthetic.grad_group_step(s, "cuda") for s in range(3))
+    run_group_steps([1] * 64, [16] * 64, hs_steps)
+
+
+def test_decoder_reduced_sizes():
+    """Every weight / activation / gradient of a 2-layer decoder at reduced
+    widths, E4M3 + E5M2 mixed in one launch, window 16, 8 steps."""
+    sizes = dict(layers=2, hidden=256, ffn=1024, tokens=512)
+    specs = synthetic.decoder_tensor_specs(**sizes)
+    steps = ([synthetic.decoder_tensor(sp, s, "cuda") for sp in specs] for s in range(8))
+    run_group_steps([sp[2] for sp in specs], [16] * len(specs), steps)
+
+
+@pytest.mark.parametrize("headroom", [0, 1])
+def test_mx_tanh_full_size(headroom):
+    """bf16 [16384, 8192] tanh(N(0,2)) -> MX E4M3: every element byte, every
+    E8M0 byte, the clipped count; then the error statistics."""
+    x = synthetic.mx_tanh("cuda")
+    rows, cols = x.shape
+    q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+    e8 = torch.empty(rows, cols // 32, dtype=torch.uint8, device="cuda")
+    cl = torch.empty(1, dtype=torch.int64, device="cuda")
+    F.mx_cast(x, F.E4M3, headroom, q, e8, cl)
+    torch.cuda.synchronize()
+    xb = host_bits(x).reshape(rows, cols)
+    q_o, e8_o, c_o = coracle.mx_cast(xb, 0, headroom, NT)
+    assert np.array_equal(e8.cpu().numpy(), e8_o)
+    assert np.array_equal(q.cpu().numpy(), q_o)
+    assert int(cl.item()) == c_o
+    if headroom == 1:
+        assert c_o == 0
+    out = torch.empty(3, dtype=torch.float64, device="cuda")
+    F.mx_error_stats(x, q, e8, F.E4M3, out)
+    mse, bias, n = out.cpu().tolist()
+    mse_o, bias_o, n_o = coracle.mx_stats(xb, q_o, e8_o, 0, NT)
+    assert int(n) == n_o
+    assert abs(mse - mse_o) <= 1e-6 * mse_o
+    assert abs(bias - bias_o) <= 1e-6 * max(abs(bias_o), mse_o ** 0.5)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_mx_edge_values(fmt, dtype):
+    """Zero blocks, NaN / Inf blocks, subnormal and huge blocks, ragged row
+    counts, fp32 and bf16, both formats, headroom 0..2."""
+    rng = np.random.default_rng(41)
+    rows, cols = 37, 96
+    v = rng.standard_normal((rows, cols)) * np.exp(rng.uniform(-40, 40, size=(rows, 1)))
+    v[0, :32] = 0.0
+    v[0, 5] = -0.0
+    v[1, 7] = np.nan
+    v[2, 40] = -np.inf
+    v[3, :] *= 1e-38
+    v[4, 64:] = 3e38
+    x = torch.from_numpy(v.astype(np.float32)).to(dtype).cuda()
+    xb = host_bits(x).reshape(rows, cols)
+    for h in (0, 1, 2):
+        q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+        e8 = torch.empty(rows, cols // 32, dtype=torch.uint8, device="cuda")
+        cl = torch.empty(1, dtype=torch.int64, device="cuda")
+        F.mx_cast(x, fmt, h, q, e8, cl)
+        torch.cuda.synchronize()
+        q_o, e8_o, c_o = coracle.mx_cast(xb, fmt, h)
+        assert np.array_equal(e8.cpu().numpy(), e8_o), h
+        assert np.array_equal(q.cpu().numpy(), q_o), h
+        assert int(cl.item()) == c_o
+
+
+# ---------------------------------------------------------------------------
+# edge cases of the per-tensor path
+# ---------------------------------------------------------------------------
+
+SIZES = [0, 1, 15, 16, 17, 31, 33, 4095, 8191, 8192, 8193, 16383, 16384, 16385, 65537,
+         (1 << 20) + 3]
+
+
+def _special_tensor(n, dtype, seed):
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal(n) * np.exp(rng.uniform(-5, 5))
+    if n > 20:
+        v[3] = -0.0
+        v[7] = 0.0
+        v[11] = 1e-42
+        v[13] = -1e-45
+    return torch.from_numpy(v.astype(np.float32)).to(dtype).cuda()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("window", [0, 3])
+def test_sizes_and_special_values(dtype, window):
+    """Empty, tiny, ragged and chunk-boundary sizes; current scaling in one
+    CTA and with the pre-pass; delayed steps; signed zeros, subnormals."""
+    for fmt in (0, 1):
+        for n in SIZES:
+            g = F.ScaledCast(fmt, window=window, margin=1 if window else 0)
+            o = policy.ScalingState(fmt, window=window, margin=1 if window else 0)
+            xs = [_special_tensor(n, dtype, 100 + n + k) * (4.0 ** k) for k in range(3)]
+            run_steps(g, o, xs)
+            g.close()
+
+
+def test_nonfinite_inputs():
+    """NaN and Inf in the tensor: NaN -> sign|0x7F, Inf saturates and counts,
+    amax becomes NaN, the next exponent is kept."""
+    for dtype in (torch.bfloat16, torch.float32):
+        for fmt in (0, 1):
+            g = F.ScaledCast(fmt, window=2)
+            o = policy.ScalingState(fmt, window=2)
+            base = _special_tensor(50000, dtype, 7)
+            a = base.clone()
+            a[100] = float("inf")
+            a[200] = float("-inf")
+            b = base.clone()
+            b[300] = float("nan")
+            b[301] = -float("nan")
+            run_steps(g, o, [base, a, b, base, base])
+            g.close()
+
+
+def test_hysteresis_sequence():
+    rng = np.random.default_rng(9)
+    xs = [torch.from_numpy((rng.standard_normal(30000) * s).astype(np.float32)).cuda()
+          for s in (1, 0.5, 0.26, 0.1, 0.05, 1, 3, 0.2)]
+    for h in (1, 2):
+        g = F.ScaledCast(0, window=1, hysteresis=h)
+        o = policy.ScalingState(0, window=1, hysteresis=h)
+        run_steps(g, o, xs)
+        g.close()
+
+
+def test_group_over_512_tensors_mixed():
+    """600 tensors of mixed size / dtype / format / window (two launches),
+    several steps."""
+    rng = np.random.default_rng(17)
+    cnt = 600
+    fmts = [int(f) for f in rng.integers(0, 2, cnt)]
+    wins = [int(w) for w in rng.integers(0, 5, cnt)]
+    sizes = [int(s) for s in rng.choice([1, 17, 1000, 8192, 16385, 40000], cnt)]
+    dts = [torch.bfloat16 if rng.integers(0, 2) else torch.float32 for _ in range(cnt)]
+    steps = [[_special_tensor(n, d, 1000 * s + i) for i, (n, d) in enumerate(zip(sizes, dts))]
+             for s in range(3)]
+    run_group_steps(fmts, wins, steps)
+
+
+def test_resume_equals_continuous():
+    """16 steps straight == 8 steps, save history + exponent, restore into a
+    fresh handle, 8 more steps (byte for byte)."""
+    xs = [synthetic.spike_step(s, "cuda", shape=(512, 1024)) for s in range(16)]
+    a = F.ScaledCast(0, window=4, margin=1)
+    full = [a(x)[0].cpu() for x in xs]
+    b = F.ScaledCast(0, window=4, margin=1)
+    part = [b(x)[0].cpu() for x in xs[:8]]
+    saved, (prev_e, _) = b.history(), b.state()
+    c = F.ScaledCast(0, window=4, margin=1)
+    c.set_history(saved, prev_e)
+    part += [c(x)[0].cpu() for x in xs[8:]]
+    assert all(torch.equal(u, v) for u, v in zip(full, part))
+    for g in (a, b, c):
+        g.close()
+
+
+def test_per_tensor_error_stats():
+    x = synthetic.spike_step(9, "cuda", shape=(1024, 1024))
+    for fmt in (0, 1):
+        g = F.ScaledCast(fmt, window=1)
+        g(x * 0.125)                          # history from a smaller tensor: step 2 clips
+        q, sinv, _, _ = g(x)
+        out = torch.empty(3, dtype=torch.float64, device="cuda")
+        F.fp8q_error_stats(x, q, fmt, sinv, out)
+        mse, bias, n = out.cpu().tolist()
+        e = -int(np.log2(sinv.item()))
+        mse_o, bias_o, n_o = coracle.stats(host_bits(x), q.cpu().numpy().reshape(-1), fmt, e, NT)
+        assert int(n) == n_o
+        assert abs(mse - mse_o) <= 1e-6 * mse_o
+        assert abs(bias - bias_o) <= 1e-6 * max(abs(bias_o), mse_o ** 0.5)
+        g.close()
+
+
+def test_argument_errors():
+    h = F.fp8q_create(0, 4)
+    x = torch.randn(1000, device="cuda")
+    q = torch.empty(1001, dtype=torch.uint8, device="cuda")
+    with pytest.raises(F.Fp8qError) as ei:
+        F.fp8q_cast(h, x[1:], q)                # misaligned input
+    assert ei.value.status == -2
+    with pytest.raises(F.Fp8qError) as ei:
+        F.fp8q_cast_multi([h, h], [x, x], [q, q])   # same handle twice
+    assert ei.value.status == -1
+    with pytest.raises(F.Fp8qError):
+        F.fp8q_set_history(h, [1.0] * 5)        # more than the window
+    F.fp8q_destroy(h)
