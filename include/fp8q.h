@@ -84,7 +84,8 @@ enum {
   FP8Q_ECUDA = -4,    /* a CUDA call failed; see fp8q_last_cuda_error()     */
   FP8Q_EHANDLE = -5,  /* null or destroyed handle                           */
   FP8Q_ENOMEM = -6,   /* device or host allocation failed                   */
-  FP8Q_EDEVICE = -7   /* handle used with another device current            */
+  FP8Q_EDEVICE = -7,  /* handle used with another device current            */
+  FP8Q_ESIZE = -8     /* size above the limit of a fixed-size scratch area  */
 };
 
 /* Largest history window a handle may keep. */
@@ -179,6 +180,34 @@ FP8Q_API int fp8q_error_stats(const void* x, int dtype, int64_t n, const uint8_t
 FP8Q_API int mx_error_stats(const void* x, int dtype, int64_t rows, int64_t cols,
                             const uint8_t* q, const uint8_t* e8m0, int format, double* d_out,
                             void* stream);
+
+/* Allocation-free variant of fp8q_error_stats (this entry point has no
+ * counterpart on the pages; it exists for callers of this library that
+ * cannot allocate device memory).  Some callers cannot call cudaMalloc or
+ * cudaMallocAsync at the point where they want the statistics: a framework
+ * whose caching allocator already owns all of the device's memory (an extra
+ * allocation fails or forces the pool to give memory back), a diagnostic
+ * that runs right after an out-of-memory error, or a latency-bound loop in
+ * which an allocation may synchronize the device.  fp8q_error_stats
+ * allocates its per-CTA partial sums with cudaMallocAsync; this entry point
+ * takes them from a fixed array in the library's device memory instead and
+ * calls no allocating routine.
+ *   Arguments, outputs and results: as fp8q_error_stats (the fp64 sums are
+ *   added in a different order, so results may differ in the last bits).
+ *   n must be <= FP8Q_STATS_NOALLOC_MAX_N, else FP8Q_ESIZE.
+ *   The array (FP8Q_STATS_NOALLOC_ROWS rows of 3 doubles, 96 KiB) is held
+ *   by every GPU that loads the library until the process exits.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   All calls share the one array, which keeps the contents of the last
+ *   call: calls that overlap on the GPU (two streams, or two host threads)
+ *   race on it and give wrong results, so order them on one stream. */
+#define FP8Q_STATS_NOALLOC_ROWS 4096
+#define FP8Q_STATS_NOALLOC_MAX_N (4096LL << 20)
+FP8Q_API int fp8q_error_stats_noalloc(const void* x, int dtype, int64_t n, const uint8_t* q,
+                                      int format, const float* d_scale_inv, double* d_out,
+                                      void* stream);
 
 /* Name of a status code (static string). */
 FP8Q_API const char* fp8q_strerror(int code);

@@ -24,6 +24,10 @@ static int fail_cuda(cudaError_t e) {
   return FP8Q_ECUDA;
 }
 
+int record_cuda_error(cudaError_t e) { return fail_cuda(e); }
+
+void note_launches(int k) { g_launches += k; }
+
 int device_of_current() {
   int d = 0;
   cudaGetDevice(&d);
@@ -97,6 +101,7 @@ FP8Q_API const char* fp8q_strerror(int code) {
     case FP8Q_EHANDLE: return "invalid handle";
     case FP8Q_ENOMEM: return "out of memory";
     case FP8Q_EDEVICE: return "handle used on another device";
+    case FP8Q_ESIZE: return "size above the fixed scratch limit";
     default: return "unknown status";
   }
 }

@@ -74,6 +74,8 @@ cudaError_t launch_stats(const void* x, int dtype, int64_t n, const uint8_t* q, 
                          cudaStream_t s, int* launches);
 
 int sm_count(int device);
+int record_cuda_error(cudaError_t e);   // keeps the text, returns FP8Q_ECUDA
+void note_launches(int k);              // adds to fp8q_launch_count()
 int device_of_current();
 
 }  // namespace fp8q

@@ -10,6 +10,8 @@
 // result does not depend on scheduling.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "fp8q_device.cuh"
 #include "fp8q_internal.cuh"
 
@@ -131,3 +133,75 @@ cudaError_t launch_stats(const void* x, int dtype, int64_t n, const uint8_t* q, 
 }
 
 }  // namespace fp8q
+
+// ---- allocation-free variant of the per-tensor statistics ------------------
+//
+// For callers that cannot allocate device memory when they want the
+// statistics (their own allocator owns the device's memory, they run after
+// an out-of-memory error, or an allocation would stall a latency-bound
+// loop).  The per-CTA partial sums go to this fixed array instead of a
+// cudaMallocAsync block: one CTA per slab of 2^20 elements, one row of three
+// doubles per CTA, so n <= 4096 * 2^20.  Every row the final kernel reads is
+// written earlier in the same call, so nothing needs clearing between calls.
+namespace fp8q {
+
+constexpr int kNoAllocRows = FP8Q_STATS_NOALLOC_ROWS;
+constexpr int64_t kNoAllocSlab = int64_t(1) << 20;
+static_assert(FP8Q_STATS_NOALLOC_MAX_N == kNoAllocRows * kNoAllocSlab, "limit and rows disagree");
+
+static __device__ __align__(256) double g_stats_scratch[3 * kNoAllocRows];
+
+// Device address of g_stats_scratch for each device, looked up once with
+// that device current (the host-side name is only a stand-in).
+static std::mutex g_scratch_mu;
+static double* g_scratch_ptr[128] = {};
+
+static cudaError_t stats_scratch(int device, double** out) {
+  if (device < 0 || device >= 128) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_ptr[device] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_stats_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[device] = static_cast<double*>(p);
+  }
+  *out = g_scratch_ptr[device];
+  return cudaSuccess;
+}
+
+}  // namespace fp8q
+
+extern "C" FP8Q_API int fp8q_error_stats_noalloc(const void* x, int dtype, int64_t n,
+                                                 const uint8_t* q, int format,
+                                                 const float* d_scale_inv, double* d_out,
+                                                 void* stream) {
+  using namespace fp8q;
+  if (dtype != FP8Q_F32 && dtype != FP8Q_BF16) return FP8Q_EDTYPE;
+  if (format != FP8Q_E4M3 && format != FP8Q_E5M2) return FP8Q_EDTYPE;
+  if (n < 0 || !d_out || !d_scale_inv || (n > 0 && (!x || !q))) return FP8Q_EINVAL;
+  if (n > FP8Q_STATS_NOALLOC_MAX_N) return FP8Q_ESIZE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (n == 0) {
+    const cudaError_t e = cudaMemsetAsync(d_out, 0, 3 * sizeof(double), s);
+    return e == cudaSuccess ? FP8Q_OK : record_cuda_error(e);
+  }
+  double* partial = nullptr;
+  cudaError_t e = stats_scratch(device_of_current(), &partial);
+  if (e != cudaSuccess) return record_cuda_error(e);
+  const int grid = (int)((n + kNoAllocSlab - 1) / kNoAllocSlab);
+  const int key = (dtype == FP8Q_BF16 ? 1 : 0) | (format == FP8Q_E5M2 ? 2 : 0);
+  switch (key) {
+    case 0: launch_partial<FP8Q_F32, FP8Q_E4M3, false>(x, n, q, d_scale_inv, nullptr, partial, grid, s); break;
+    case 1: launch_partial<FP8Q_BF16, FP8Q_E4M3, false>(x, n, q, d_scale_inv, nullptr, partial, grid, s); break;
+    case 2: launch_partial<FP8Q_F32, FP8Q_E5M2, false>(x, n, q, d_scale_inv, nullptr, partial, grid, s); break;
+    default: launch_partial<FP8Q_BF16, FP8Q_E5M2, false>(x, n, q, d_scale_inv, nullptr, partial, grid, s); break;
+  }
+  e = cudaGetLastError();
+  if (e == cudaSuccess) {
+    stats_final_kernel<<<1, 32, 0, s>>>(partial, grid, d_out);
+    e = cudaGetLastError();
+  }
+  note_launches(2);
+  return e == cudaSuccess ? FP8Q_OK : record_cuda_error(e);
+}
+

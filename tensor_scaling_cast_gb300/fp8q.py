@@ -22,7 +22,7 @@ NO_EXP = -(2 ** 31)
 MAX_WINDOW = 256
 
 _STATUS = {0: "FP8Q_OK", -1: "FP8Q_EINVAL", -2: "FP8Q_EALIGN", -3: "FP8Q_EDTYPE", -4: "FP8Q_ECUDA",
-           -5: "FP8Q_EHANDLE", -6: "FP8Q_ENOMEM", -7: "FP8Q_EDEVICE"}
+           -5: "FP8Q_EHANDLE", -6: "FP8Q_ENOMEM", -7: "FP8Q_EDEVICE", -8: "FP8Q_ESIZE"}
 
 
 class Fp8qError(RuntimeError):
@@ -56,13 +56,14 @@ def load() -> ctypes.CDLL:
     L.fp8q_reset.argtypes = [p]
     L.fp8q_error_stats.argtypes = [p, i, i64, p, i, p, p, p]
     L.mx_error_stats.argtypes = [p, i, i64, i64, p, p, i, p, p]
+    L.fp8q_error_stats_noalloc.argtypes = [p, i, i64, p, i, p, p, p]
     L.fp8q_strerror.argtypes = [i]
     L.fp8q_strerror.restype = ctypes.c_char_p
     L.fp8q_last_cuda_error.restype = ctypes.c_char_p
     L.fp8q_launch_count.restype = ctypes.c_longlong
     for name in ("fp8q_create", "fp8q_destroy", "fp8q_cast", "fp8q_cast_multi", "mx_cast",
                  "fp8q_amax_history", "fp8q_scale_state", "fp8q_set_history", "fp8q_reset",
-                 "fp8q_error_stats", "mx_error_stats"):
+                 "fp8q_error_stats", "mx_error_stats", "fp8q_error_stats_noalloc"):
         getattr(L, name).restype = i
     _lib = L
     return L
@@ -172,6 +173,15 @@ def fp8q_error_stats(x: torch.Tensor, q: torch.Tensor, fmt: int, scale_inv: torc
                      out: torch.Tensor, stream=None):
     _check(load().fp8q_error_stats(_ptr(x), _dtype(x), x.numel(), _ptr(q), fmt, _ptr(scale_inv),
                                    _ptr(out), _stream(stream)), "fp8q_error_stats")
+
+
+def fp8q_error_stats_noalloc(x: torch.Tensor, q: torch.Tensor, fmt: int, scale_inv: torch.Tensor,
+                             out: torch.Tensor, stream=None):
+    """fp8q_error_stats without any device allocation (fixed library
+    scratch; n <= 2^32; calls must not overlap on the GPU)."""
+    _check(load().fp8q_error_stats_noalloc(_ptr(x), _dtype(x), x.numel(), _ptr(q), fmt,
+                                           _ptr(scale_inv), _ptr(out), _stream(stream)),
+           "fp8q_error_stats_noalloc")
 
 
 def mx_error_stats(x: torch.Tensor, q: torch.Tensor, e8m0: torch.Tensor, fmt: int,
