@@ -1,18 +1,21 @@
 """Throughput of the scaled FP8 casts on GB300 (GB/s moved, read + write).
 
-Default workload, one step = the whole hot path over one batch:
+Default workload (``--workload decoder``), one step = the whole hot path over
+one batch:
   * the per-step cast of every weight, activation and activation gradient of
     a 24-layer decoder (hidden 2048, FFN 8192, batch 4 x seq 4096): 384 bf16
     tensors, 14,092,861,440 elements, weights and activations to E4M3,
     gradients to E5M2, per-tensor max-window scaling (window 16), in one
     grouped launch (fp8q_cast_multi);
   * the MX E4M3 cast (OCP rule) of the bf16 [16384, 8192] tanh activations.
-Algorithmic bytes: 3 B per element for the per-tensor cast (2 read + 1
-written), 3.03125 B per element for MX (+1 E8M0 byte per 32).
+Algorithmic bytes: 3 B per element for a bf16 per-tensor cast (2 read + 1
+written), 5 B for fp32, 3.03125 B per element for bf16 MX (+1 E8M0 byte per
+32).  The other workloads (current, spike, grad, mx, single) measure the
+remaining configurations and small profiling cases with the same JSON line.
 
 Run: python bench.py [--steps K] [--warmup W] [--impl ours|reference]
-     [--workload decoder|single|mx] [--n N]  (torchrun for --gpus N > 1:
-     replicas, one full workload per GPU).
+     [--workload decoder|current|spike|grad|mx|single] [--n N]
+(torchrun for --gpus N > 1: replicas, one full workload per GPU).
 """
 from __future__ import annotations
 
@@ -29,7 +32,6 @@ sys.path.insert(0, ROOT)
 
 METRIC = "FP8 scaled-cast GB/s (read+write) and fraction of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
-L2_BYTES = 129 * 2 ** 20
 
 
 def parse():
@@ -38,28 +40,60 @@ def parse():
     p.add_argument("--steps", type=int, default=300)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="decoder", choices=["decoder", "single", "mx"])
+    p.add_argument("--workload", default="decoder",
+                   choices=["decoder", "current", "spike", "grad", "mx", "single"])
     p.add_argument("--n", type=int, default=1 << 26, help="elements for --workload single")
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--cpu-one-core", action="store_true",
+                   help="also time the oracle on a single thread")
     return p.parse_args()
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """Largest value over all ranks (the slowest rank's time); identity for
+    one process.  device: where the collective's tensor lives (cuda for
+    NCCL, cpu for gloo)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
-        with open(path) as f:
-            d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def cast_bytes(x) -> int:
+    return x.numel() * (x.element_size() + 1)
+
+
+def mx_bytes(x) -> int:
+    return x.numel() * (x.element_size() + 1) + x.numel() // 32
+
+
 # ---------------------------------------------------------------------------
-# workload construction (device-resident inputs and outputs)
+# workloads: parts launched in order each step, device-resident buffers
 # ---------------------------------------------------------------------------
+
+class Part:
+    """One launch (or grouped launch) of a step."""
+
+    def __init__(self, name, kernel, nbytes, run, inputs, outputs):
+        self.name, self.kernel, self.bytes = name, kernel, nbytes
+        self.run = run              # run(k): enqueue on the current stream
+        self.inputs = inputs        # inputs(k) -> device tensors read at step k
+        self.outputs = outputs      # outputs(k) -> device tensors written at step k
+
 
 class Workload:
     def __init__(self, kind: str, n: int, device):
@@ -67,56 +101,91 @@ class Workload:
 
         from tensor_scaling_cast_gb300 import fp8q as F
         from tensor_scaling_cast_gb300 import synthetic as S
-        self.kind, self.F, self.torch = kind, F, torch
-        self.xs, self.fmts, self.handles = [], [], []
-        self.mx_x = None
+        self.kind, self.device = kind, device
+        self.handles = []
+        self.parts: list[Part] = []
+        self.oracle_jobs = []       # (callable(nthreads) -> bytes) for the CPU baseline
+        dev = device
+
+        def grouped(name, xs, fmts, window, margin=0):
+            hs = [F.fp8q_create(f, window, margin, 0) for f in fmts]
+            self.handles += hs
+            qs = [torch.empty(x.numel(), dtype=torch.uint8, device=dev) for x in xs]
+            m = len(xs)
+            outs = [torch.empty(m, dtype=torch.float32, device=dev),
+                    torch.empty(m, dtype=torch.float32, device=dev),
+                    torch.empty(m, dtype=torch.int64, device=dev)]
+            run = lambda k: F.fp8q_cast_multi(hs, xs, qs, *outs)
+            self.parts.append(Part(name, "cast_group_kernel", sum(cast_bytes(x) for x in xs), run,
+                                   lambda k: xs, lambda k: qs + outs))
+            for x, f in zip(xs, fmts):
+                self.oracle_jobs.append(("cast", x, f, window, margin))
+
+        def mx(name, x, headroom):
+            r, c = x.shape
+            q = torch.empty(r, c, dtype=torch.uint8, device=dev)
+            e8 = torch.empty(r, c // 32, dtype=torch.uint8, device=dev)
+            cl = torch.empty(1, dtype=torch.int64, device=dev)
+            run = lambda k: F.mx_cast(x, F.E4M3, headroom, q, e8, cl)
+            self.parts.append(Part(name, "mx_kernel", mx_bytes(x), run, lambda k: [x],
+                                   lambda k: [q, e8, cl]))
+            self.oracle_jobs.append(("mx", x, 0, headroom, 0))
+
         if kind == "decoder":
-            self.specs = S.decoder_tensor_specs()
-            for sp in self.specs:
-                self.xs.append(S.decoder_tensor(sp, 0, device))
-                self.fmts.append(sp[2])
-            self.mx_x = S.mx_tanh(device)
+            specs = S.decoder_tensor_specs()
+            xs = [S.decoder_tensor(sp, 0, dev) for sp in specs]
+            grouped("grouped_cast", xs, [sp[2] for sp in specs], 16)
+            mx("mx_cast", S.mx_tanh(dev), 0)
             self.name = ("decoder_1b1 per-step cast (384 bf16 tensors, 14,092,861,440 elements; "
                          "E4M3 weights/activations, E5M2 gradients; max-window 16) + MX E4M3 OCP "
                          "cast of bf16 [16384, 8192] tanh(N(0,2))")
-        elif kind == "single":
-            g = torch.Generator(device=device)
-            g.manual_seed(1)
-            self.xs.append(torch.randn(n, generator=g, device=device).to(torch.bfloat16))
-            self.fmts.append(F.E4M3)
-            self.name = f"single bf16 tensor of {n} elements, E4M3, max-window 16"
+        elif kind == "grad":
+            xs = S.grad_group_step(1, dev)
+            grouped("grouped_cast", xs, [1] * len(xs), 16)
+            self.name = (f"grad_group: 64 bf16 tensors ({sum(x.numel() for x in xs)} elements), "
+                         "E5M2, max-window 16, one grouped launch")
+        elif kind == "mx":
+            x = S.mx_tanh(dev)
+            mx("mx_cast_ocp", x, 0)
+            mx("mx_cast_headroom1", x, 1)
+            self.name = "MX E4M3 of bf16 [16384, 8192] tanh(N(0,2)): OCP rule and +1 headroom"
+        elif kind == "spike":
+            seq = [S.spike_step(s, dev) for s in range(S.SPIKE_STEPS)]
+            for name, w, m in (("most_recent_w1", 1, 0), ("max_window_w16_m1", 16, 1)):
+                g = F.ScaledCast(F.E4M3, w, m)
+                self.handles.append(g)
+                q = torch.empty(seq[0].numel(), dtype=torch.uint8, device=dev)
+                run = (lambda g, q: lambda k: g(seq[k % len(seq)], q))(g, q)
+                self.parts.append(Part(name, "cast_group_kernel", cast_bytes(seq[0]), run,
+                                       lambda k: [seq[k % len(seq)]], (lambda q: lambda k: [q])(q)))
+                self.oracle_jobs.append(("cast", seq[0], 0, w, m))
+            self.name = ("spike_seq: bf16 [4096, 4096] E4M3, inputs rotating over the 16 steps "
+                         "(512 MiB), most-recent and max-window-16 (margin 1) per step")
+        elif kind == "current":
+            x = S.current_4096(dev)
+            g = F.ScaledCast(F.E4M3, 0, 0)
+            self.handles.append(g)
+            q = torch.empty(x.numel(), dtype=torch.uint8, device=dev)
+            self.parts.append(Part("current_scaling", "cast_group_kernel", 2 * 4 * x.numel() + x.numel(),
+                                   lambda k: g(x, q), lambda k: [x], lambda k: [q]))
+            self.oracle_jobs.append(("cast", x, 0, 0, 0))
+            self.name = "current_4096: fp32 [4096] N(0,1), E4M3, current scaling (latency)"
         else:
-            self.mx_x = S.mx_tanh(device)
-            self.name = "MX E4M3 OCP cast of bf16 [16384, 8192] tanh(N(0,2))"
-        self.handles = [F.fp8q_create(f, 16, 0, 0) for f in self.fmts]
-        self.qs = [torch.empty(x.numel(), dtype=torch.uint8, device=device) for x in self.xs]
-        m = max(1, len(self.xs))
-        self.sinv = torch.empty(m, dtype=torch.float32, device=device)
-        self.amax = torch.empty(m, dtype=torch.float32, device=device)
-        self.clipped = torch.empty(m, dtype=torch.int64, device=device)
-        if self.mx_x is not None:
-            r, c = self.mx_x.shape
-            self.mx_q = torch.empty(r, c, dtype=torch.uint8, device=device)
-            self.mx_e8 = torch.empty(r, c // 32, dtype=torch.uint8, device=device)
-            self.mx_clip = torch.empty(1, dtype=torch.int64, device=device)
-        self.cast_elems = sum(x.numel() for x in self.xs)
-        self.mx_elems = 0 if self.mx_x is None else self.mx_x.numel()
-        self.cast_bytes = 3 * self.cast_elems
-        self.mx_bytes = 0 if self.mx_x is None else self.mx_elems * 2 + self.mx_elems + self.mx_elems // 32
-        self.step_bytes = self.cast_bytes + self.mx_bytes
+            g = torch.Generator(device=dev)
+            g.manual_seed(1)
+            x = torch.randn(n, generator=g, device=dev).to(torch.bfloat16)
+            grouped("cast", [x], [F.E4M3], 16)
+            self.name = f"single bf16 tensor of {n} elements, E4M3, max-window 16"
+        self.step_bytes = sum(p.bytes for p in self.parts)
+        self.elements = None
 
-    def step(self, ev=None):
-        F = self.F
+    def step(self, k, ev=None):
+        for i, p in enumerate(self.parts):
+            if ev is not None:
+                ev[i].record()
+            p.run(k)
         if ev is not None:
-            ev[0].record()
-        if self.xs:
-            F.fp8q_cast_multi(self.handles, self.xs, self.qs, self.sinv, self.amax, self.clipped)
-        if ev is not None:
-            ev[1].record()
-        if self.mx_x is not None:
-            F.mx_cast(self.mx_x, F.E4M3, 0, self.mx_q, self.mx_e8, self.mx_clip)
-        if ev is not None:
-            ev[2].record()
+            ev[len(self.parts)].record()
 
 
 # ---------------------------------------------------------------------------
@@ -140,7 +209,8 @@ class Clocks:
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0: float, t1: float):
+        """Samples taken between host times t0 and t1 (the timed region)."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -160,54 +230,110 @@ class Clocks:
                 if v.lower() == "active":
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window_s": round(t1 - t0, 3)}
 
 
 # ---------------------------------------------------------------------------
 # the oracle on the host cores (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def cpu_oracle_sample(seconds: float, inputs=None):
-    """Cast decoder_1b1 tensors (step 0 = current scaling, then a delayed
-    step) through the oracle until about `seconds` of work; returns
-    (GB/s, cores, description)."""
+def _bits(x):
     import numpy as np
     import torch
+    x = x.detach().contiguous().cpu()
+    if x.dtype == torch.bfloat16:
+        return x.view(torch.int16).numpy().view(np.uint16)
+    return x.view(torch.int32).numpy().view(np.uint32)
+
+
+def oracle_time(jobs, seconds: float, nthreads: int):
+    """Run the oracle over the workload's tensors (a delayed-scaling cast per
+    per-tensor job after one window-filling cast; an MX cast per MX job),
+    round-robin, until about `seconds` of timed work.  Returns
+    (GB/s, description)."""
+    from oracle import coracle, policy
+    coracle.build()
+    done, elapsed, count, i, names = 0, 0.0, 0, 0, set()
+    host = {}
+    while elapsed < seconds and i < 64 * len(jobs):
+        kind, x, fmt, a, b = jobs[i % len(jobs)]
+        key = id(x)
+        if key not in host:
+            host[key] = _bits(x)
+        xb = host[key]
+        if kind == "cast":
+            st = policy.ScalingState(fmt, a, b)
+            if a > 0:
+                st.step(xb.reshape(-1), nthreads)          # fill the window (not timed)
+            t0 = time.perf_counter()
+            st.step(xb.reshape(-1), nthreads)
+            elapsed += time.perf_counter() - t0
+            done += xb.size * (xb.itemsize + 1)
+        else:
+            t0 = time.perf_counter()
+            coracle.mx_cast(xb, 0, a, nthreads)
+            elapsed += time.perf_counter() - t0
+            done += xb.size * (xb.itemsize + 1) + xb.size // 32
+        names.add(kind)
+        count += 1
+        i += 1
+    desc = (f"oracle.c: {count} casts ({'/'.join(sorted(names))}) of this workload's tensors, "
+            f"{done / 1e9:.2f} GB moved, {elapsed:.1f} s on {nthreads} thread(s)")
+    return done / elapsed / 1e9, desc
+
+
+def run_reference(args, rank: int):
+    """The reference arm: the CPU oracle as it stands, on the host cores, no
+    GPU.  Each of the W + K steps casts a bounded slice of the decoder_1b1
+    workload (round-robin over one layer's 16 tensors, delayed scaling with
+    a filled window), sized so the whole run takes about a minute."""
+    if rank != 0:
+        return
+    import numpy as np
 
     from oracle import coracle, policy
     from tensor_scaling_cast_gb300 import synthetic as S
     coracle.build()
     cores = os.cpu_count() or 1
-    specs = S.decoder_tensor_specs()
-    done_bytes, done_elems, elapsed, names = 0, 0, 0.0, []
-    i = 0
-    while elapsed < seconds and i < len(specs):
-        sp = specs[i]
-        x = inputs[i] if inputs is not None else S.decoder_tensor(sp, 0, "cpu")
-        xb = x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1)
-        st = policy.ScalingState(sp[2], 16)
-        st.step(xb, cores)                       # fill the window (not timed)
+    specs = S.decoder_tensor_specs()[:16]
+    xs, states = {}, {}
+
+    def tensor(i):                              # generated and window-filled on first use
+        if i not in xs:
+            xs[i] = _bits(S.decoder_tensor(specs[i], 0, "cpu")).reshape(-1)
+            st = policy.ScalingState(specs[i][2], 16)
+            st.step(xs[i][: 1 << 20], cores)
+            states[i] = st
+        return xs[i], states[i]
+
+    x0, _ = tensor(0)
+    t0 = time.perf_counter()
+    policy.ScalingState(0, 16).step(x0[: 1 << 22], cores)
+    rate = (1 << 22) / max(1e-6, time.perf_counter() - t0)          # elements / s
+    budget = max(2.0, 4 * args.cpu_seconds)
+    per_step = int(min(1 << 26, max(1 << 16, rate * budget / (args.steps + args.warmup))))
+    done, elapsed = 0, 0.0
+    for k in range(args.warmup + args.steps):
+        i = k % len(specs)
+        x, st = tensor(i)
+        off = ((k // len(specs)) * per_step) % max(1, x.size - per_step)
+        sl = np.ascontiguousarray(x[off: off + per_step])
         t0 = time.perf_counter()
-        st.step(xb, cores)                       # one delayed-scaling cast
-        elapsed += time.perf_counter() - t0
-        done_bytes += 3 * xb.size
-        done_elems += xb.size
-        names.append(sp[0])
-        i += 1
-    desc = (f"oracle.c max-window cast of {len(names)} decoder_1b1 tensors ({names[0]}..{names[-1]}), "
-            f"{done_elems} elements, {elapsed:.1f} s on {cores} threads")
-    return done_bytes / elapsed / 1e9, cores, desc
-
-
-def run_reference(args, rank: int):
-    if rank != 0:
-        return
-    gbs, cores, desc = cpu_oracle_sample(max(3.0, args.cpu_seconds))
+        st.step(sl, cores)
+        dt = time.perf_counter() - t0
+        if k >= args.warmup:
+            elapsed += dt
+            done += sl.size * 3
+    gbs = done / elapsed / 1e9
+    desc = (f"oracle.c delayed-scaling cast, {args.steps} timed steps of up to {per_step} elements "
+            f"(slices of decoder_1b1 layer-0 tensors, round-robin), {elapsed:.1f} s on {cores} threads")
     line = {"metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "impl": "reference",
-            "config": {"workload": "decoder_1b1 per-step cast (sample, see cpu_baseline)",
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * elapsed / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": "decoder_1b1 per-step cast, bounded slices (see cpu_baseline)",
                        "parallelism": "replicas"},
             "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": cores,
                              "kind": "oracle", "sample": desc},
@@ -237,152 +363,137 @@ def run_ours(args, rank: int, world: int):
     F.load()
     W = Workload(args.workload, args.n, dev)
     torch.cuda.synchronize()
-    for _ in range(max(3, args.warmup)):
-        W.step()
-    torch.cuda.synchronize()
-
-    # device-resident timed region
-    K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     clocks = Clocks(local)
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.5)                            # sampler up before the GPU work starts
+    warm = max(3, args.warmup)
+    for k in range(warm):
+        W.step(k)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    P = len(W.parts)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(P + 1)] for _ in range(K)]
     if world > 1:
         dist.barrier()
-    torch.cuda.synchronize()
     l0 = F.launch_count()
+    host_t0 = time.time()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record()
     for k in range(K):
-        W.step(evs[k])
+        W.step(warm + k, evs[k])
     t_end.record()
     torch.cuda.synchronize()
+    host_t1 = time.time()
     launches = F.launch_count() - l0
+    clk = clocks.stop(host_t0, host_t1)
     if world > 1:
         dist.barrier()
-    clk = clocks.stop()
-    ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     ms_step = ms / K
-    cast_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) if W.xs else 0.0
-    mx_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) if W.mx_x is not None else 0.0
     value = world * W.step_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_kind = peaks()
 
-    # dominant kernel roofline
-    if W.xs:
-        dom, dom_ms, dom_bytes = "cast_group_kernel", cast_ms, W.cast_bytes
-    else:
-        dom, dom_ms, dom_bytes = "mx_kernel", mx_ms, W.mx_bytes
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     parts = {}
-    if W.xs:
-        parts["grouped_cast"] = {"ms": round(cast_ms, 4), "bytes": W.cast_bytes,
-                                 "GB/s": round(W.cast_bytes / (cast_ms * 1e-3) / 1e9, 1),
-                                 "frac": round(W.cast_bytes / (cast_ms * 1e-3) / 1e9 / peak, 4)}
-    if W.mx_x is not None:
-        parts["mx_cast"] = {"ms": round(mx_ms, 4), "bytes": W.mx_bytes,
-                            "GB/s": round(W.mx_bytes / (mx_ms * 1e-3) / 1e9, 1),
-                            "frac": round(W.mx_bytes / (mx_ms * 1e-3) / 1e9 / peak, 4)}
+    for i, p in enumerate(W.parts):
+        pm = statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+        gbs = p.bytes / (pm * 1e-3) / 1e9
+        parts[p.name] = {"kernel": p.kernel, "ms": round(pm, 5), "bytes": p.bytes,
+                         "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    dom = max(W.parts, key=lambda p: parts[p.name]["ms"])
+    dpart = parts[dom.name]
 
-    # end to end through the C ABI from pinned host buffers
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(W, args.e2e_steps, world, dev)
+    e2e = None if args.no_e2e else run_e2e(W, args.e2e_steps, world, dev, warm + K)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu and args.workload == "decoder":
-        gbs, cores, desc = cpu_oracle_sample(args.cpu_seconds, inputs=W.xs)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cores = os.cpu_count() or 1
+        gbs, desc = oracle_time(W.oracle_jobs, args.cpu_seconds, cores)
         cpu = {"value": round(gbs, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": desc}
+        if args.cpu_one_core:
+            g1, d1 = oracle_time(W.oracle_jobs, args.cpu_seconds, 1)
+            cpu["one_core"] = {"value": round(g1, 4), "sample": d1}
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
-            "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 4),
+            "steps": K, "warmup": warm, "ms_per_step": round(ms_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": W.name, "elements_per_step": W.cast_elems + W.mx_elems,
-                       "bytes_per_step": W.step_bytes, "io": "bf16 in, FP8 (+E8M0) out",
-                       "l2": f"inputs larger than L2 ({W.step_bytes / 1e9:.1f} GB moved per step)",
+            "config": {"workload": W.name, "bytes_per_step": W.step_bytes,
+                       "io": "bf16/fp32 in, FP8 (+E8M0) out",
+                       "l2": f"inputs larger than L2 ({W.step_bytes / 1e9:.2f} GB moved per step)"
+                       if args.workload in ("decoder", "grad", "mx", "spike", "single")
+                       else "tiny: L2-resident, latency only",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
-            "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
-                         "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+            "roofline": {"bound": "hbm", "kernel": dom.kernel, "achieved": dpart["GB/s"],
+                         "peak": peak, "unit": "GB/s", "frac": dpart["frac"],
+                         "peak_source": "measured: MEASURED_PEAKS.json hbm_gbs (copy)"
                          if peak_kind == "measured" else "fallback",
-                         "bytes_per_launch": dom_bytes, "traffic": None},
+                         "bytes_per_launch": dom.bytes, "traffic": None},
             "parts": parts,
             "gpu_launches": launches,
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        if args.workload == "current":
+            line["latency_us_per_cast"] = round(ms_step * 1e3, 2)
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(W, steps: int, world: int, dev):
+def run_e2e(W, steps: int, world: int, dev, k0: int):
     """Same step through the public API with host buffers: pinned H2D of the
-    step's inputs, the casts, D2H of every output (q, E8M0, scalars)."""
+    step's inputs, the casts, D2H of every output, all inside the timed
+    region."""
     import torch
     import torch.distributed as dist
-    F = W.F
-    h_x = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in W.xs]
-    for hx, x in zip(h_x, W.xs):
-        hx.copy_(x)
-    h_q = [torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for q in W.qs]
-    n = max(1, len(W.xs))
-    h_small = torch.empty(3 * n, dtype=torch.float32, pin_memory=True)
-    h_clip = torch.empty(n, dtype=torch.int64, pin_memory=True)
-    if W.mx_x is not None:
-        h_mx = torch.empty(W.mx_x.shape, dtype=W.mx_x.dtype, pin_memory=True)
-        h_mx.copy_(W.mx_x)
-        h_mq = torch.empty(W.mx_q.shape, dtype=torch.uint8, pin_memory=True)
-        h_me = torch.empty(W.mx_e8.shape, dtype=torch.uint8, pin_memory=True)
-        h_mc = torch.empty(1, dtype=torch.int64, pin_memory=True)
-    h2d = sum(x.numel() * x.element_size() for x in W.xs) + (0 if W.mx_x is None else W.mx_x.numel() * 2)
-    d2h = sum(q.numel() for q in W.qs) + (3 * 4 * n if W.xs else 0) + (8 * n if W.xs else 0)
-    if W.mx_x is not None:
-        d2h += W.mx_q.numel() + W.mx_e8.numel() + 8
+    mirror = {}
 
-    def one():
-        for hx, x in zip(h_x, W.xs):
-            x.copy_(hx, non_blocking=True)
-        if W.mx_x is not None:
-            W.mx_x.copy_(h_mx, non_blocking=True)
-        W.step()
-        for hq, q in zip(h_q, W.qs):
-            hq.copy_(q, non_blocking=True)
-        if W.xs:
-            h_small[0:n].copy_(W.sinv, non_blocking=True)
-            h_small[n:2 * n].copy_(W.amax, non_blocking=True)
-            h_clip.copy_(W.clipped, non_blocking=True)
-        if W.mx_x is not None:
-            h_mq.copy_(W.mx_q, non_blocking=True)
-            h_me.copy_(W.mx_e8, non_blocking=True)
-            h_mc.copy_(W.mx_clip, non_blocking=True)
+    def host_of(t):
+        if id(t) not in mirror:
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            mirror[id(t)] = h
+        return mirror[id(t)]
 
-    one()
+    def io(k):
+        ins, outs = [], []
+        for p in W.parts:
+            ins += [t for t in p.inputs(k) if id(t) not in {id(u) for u in ins}]
+            outs += p.outputs(k)
+        return ins, outs
+
+    ins0, outs0 = io(k0)
+    h2d = sum(t.numel() * t.element_size() for t in ins0)
+    d2h = sum(t.numel() * t.element_size() for t in outs0)
+
+    def one(k):
+        ins, outs = io(k)
+        for t in ins:
+            t.copy_(host_of(t), non_blocking=True)
+        W.step(k)
+        for t in outs:
+            host_of(t).copy_(t, non_blocking=True)
+
+    for k in range(k0, k0 + 2):
+        one(k)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
-    for _ in range(steps):
-        one()
+    for k in range(steps):
+        one(k0 + 2 + k)
     b.record()
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(a.elapsed_time(b), world, dev)
     return {"value": round(world * W.step_bytes / (ms / steps * 1e-3) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(ms / steps, 3), "steps": steps}
+            "ms_per_step": round(ms / steps, 3), "steps": steps,
+            "path": "pinned host -> cudaMemcpyAsync -> fp8q C ABI -> cudaMemcpyAsync -> pinned host"}
 
 
 def main():

@@ -189,6 +189,35 @@ def test_decoder_reduced_sizes():
     run_group_steps([sp[2] for sp in specs], [16] * len(specs), steps)
 
 
+def test_decoder_full_size_two_steps():
+    """The benchmark's workload at full size and in its launch
+    configuration: all 384 tensors of the 24-layer decoder (14,092,861,440
+    elements per step) in one fp8q_cast_multi call; step 0 (empty history:
+    current scaling with the pre-pass) and step 1 (max-window); every byte,
+    amax, scale_inv and clipped count compared with the oracle."""
+    specs = synthetic.decoder_tensor_specs()
+    hs = [F.fp8q_create(sp[2], 16, 0, 0) for sp in specs]
+    orc = [policy.ScalingState(sp[2], 16, 0, 0) for sp in specs]
+    n = len(specs)
+    for step in range(2):
+        xs = [synthetic.decoder_tensor(sp, step, "cuda") for sp in specs]
+        qs = [torch.empty(x.numel(), dtype=torch.uint8, device="cuda") for x in xs]
+        sinv = torch.empty(n, dtype=torch.float32, device="cuda")
+        amax = torch.empty(n, dtype=torch.float32, device="cuda")
+        clipped = torch.empty(n, dtype=torch.int64, device="cuda")
+        F.fp8q_cast_multi(hs, xs, qs, sinv, amax, clipped)
+        torch.cuda.synchronize()
+        sb, ab, cb = f32bits(sinv), f32bits(amax), clipped.cpu().numpy()
+        for i in range(n):
+            q_o, a_o, s_o, c_o, _ = orc[i].step(host_bits(xs[i]), NT)
+            assert np.array_equal(qs[i].cpu().numpy(), q_o.reshape(-1)), (step, specs[i][0])
+            assert ab[i] == a_o and sb[i] == s_o and int(cb[i]) == c_o, (step, specs[i][0])
+        del xs, qs
+        torch.cuda.empty_cache()
+    for h in hs:
+        F.fp8q_destroy(h)
+
+
 @pytest.mark.parametrize("headroom", [0, 1])
 def test_mx_tanh_full_size(headroom):
     """bf16 [16384, 8192] tanh(N(0,2)) -> MX E4M3: every element byte, every
