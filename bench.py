@@ -73,6 +73,33 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = ["tensor_scaling_cast_gb300/csrc/cast.cu", "tensor_scaling_cast_gb300/csrc/fp8q_device.cuh",
+                  "tensor_scaling_cast_gb300/csrc/fp8q_internal.cuh"]
+TRAFFIC_FILE = "profiles/traffic_cast_group_kernel_decoder_1b1.md"
+
+
+def captured_traffic():
+    """DRAM bytes of one full-size grouped launch from the committed ncu
+    capture, or None when the kernel sources changed since it was taken."""
+    import hashlib
+    try:
+        h = hashlib.sha256()
+        for f in KERNEL_SOURCES:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+        fields = {}
+        with open(os.path.join(ROOT, TRAFFIC_FILE)) as fh:
+            for line in fh:
+                if ":" in line and not line.startswith(("#", "|", " ")):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("source_sha256") == h.hexdigest():
+            return int(fields["traffic_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
 def cast_bytes(x) -> int:
     return x.numel() * (x.element_size() + 1)
 
@@ -96,13 +123,27 @@ class Part:
 
 
 class Workload:
-    def __init__(self, kind: str, n: int, device):
+    def __init__(self, kind: str, n: int, device, host_io: bool = False):
+        """host_io: inputs and outputs live in pinned host memory and the
+        kernels read / write them directly over NVLink-C2C (zero-copy)."""
         import torch
 
         from tensor_scaling_cast_gb300 import fp8q as F
         from tensor_scaling_cast_gb300 import synthetic as S
-        self.kind, self.device = kind, device
+        self.kind, self.device, self.host_io = kind, device, host_io
         self.handles = []
+
+        def io_in(t):                   # an input tensor in the chosen memory
+            if not host_io:
+                return t
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            return h
+
+        def io_out(shape, dtype):       # an output tensor in the chosen memory
+            if host_io:
+                return torch.empty(shape, dtype=dtype, pin_memory=True)
+            return torch.empty(shape, dtype=dtype, device=dev)
         self.parts: list[Part] = []
         self.oracle_jobs = []       # (callable(nthreads) -> bytes) for the CPU baseline
         dev = device
@@ -110,7 +151,8 @@ class Workload:
         def grouped(name, xs, fmts, window, margin=0):
             hs = [F.fp8q_create(f, window, margin, 0) for f in fmts]
             self.handles += hs
-            qs = [torch.empty(x.numel(), dtype=torch.uint8, device=dev) for x in xs]
+            xs = [io_in(x) for x in xs]
+            qs = [io_out((x.numel(),), torch.uint8) for x in xs]
             m = len(xs)
             outs = [torch.empty(m, dtype=torch.float32, device=dev),
                     torch.empty(m, dtype=torch.float32, device=dev),
@@ -121,34 +163,39 @@ class Workload:
             for x, f in zip(xs, fmts):
                 self.oracle_jobs.append(("cast", x, f, window, margin))
 
-        def mx(name, x, headroom):
+        def mx(name, x, headroom, rule=0, axis=0):
             r, c = x.shape
-            q = torch.empty(r, c, dtype=torch.uint8, device=dev)
-            e8 = torch.empty(r, c // 32, dtype=torch.uint8, device=dev)
+            q = io_out((r, c), torch.uint8)
+            e8 = io_out((r, c // 32) if axis == 0 else (r // 32, c), torch.uint8)
             cl = torch.empty(1, dtype=torch.int64, device=dev)
-            run = lambda k: F.mx_cast(x, F.E4M3, headroom, q, e8, cl)
-            self.parts.append(Part(name, "mx_kernel", mx_bytes(x), run, lambda k: [x],
-                                   lambda k: [q, e8, cl]))
+            run = lambda k: F.mx_cast_ex(x, F.E4M3, rule, headroom, axis, q, e8, cl)
+            self.parts.append(Part(name, "mx_kernel" if axis == 0 else "mx_colwise_kernel",
+                                   mx_bytes(x), run, lambda k: [x], lambda k: [q, e8, cl]))
             self.oracle_jobs.append(("mx", x, 0, headroom, 0))
 
         if kind == "decoder":
             specs = S.decoder_tensor_specs()
-            xs = [S.decoder_tensor(sp, 0, dev) for sp in specs]
+            xs = [io_in(S.decoder_tensor(sp, 0, dev)) for sp in specs]
             grouped("grouped_cast", xs, [sp[2] for sp in specs], 16)
-            mx("mx_cast", S.mx_tanh(dev), 0)
+            mx("mx_cast", io_in(S.mx_tanh(dev)), 0)
             self.name = ("decoder_1b1 per-step cast (384 bf16 tensors, 14,092,861,440 elements; "
                          "E4M3 weights/activations, E5M2 gradients; max-window 16) + MX E4M3 OCP "
                          "cast of bf16 [16384, 8192] tanh(N(0,2))")
         elif kind == "grad":
-            xs = S.grad_group_step(1, dev)
+            xs = [io_in(x) for x in S.grad_group_step(1, dev)]
             grouped("grouped_cast", xs, [1] * len(xs), 16)
             self.name = (f"grad_group: 64 bf16 tensors ({sum(x.numel() for x in xs)} elements), "
                          "E5M2, max-window 16, one grouped launch")
         elif kind == "mx":
-            x = S.mx_tanh(dev)
+            x = io_in(S.mx_tanh(dev))
             mx("mx_cast_ocp", x, 0)
             mx("mx_cast_headroom1", x, 1)
-            self.name = "MX E4M3 of bf16 [16384, 8192] tanh(N(0,2)): OCP rule and +1 headroom"
+            mx("mx_cast_ceil", x, 0, rule=1)
+            mx("mx_cast_nearest", x, 0, rule=2)
+            mx("mx_cast_colwise_ocp", x, 0, axis=1)
+            mx("mx_cast_colwise_ceil", x, 0, rule=1, axis=1)
+            self.name = ("MX E4M3 of bf16 [16384, 8192] tanh(N(0,2)): row-wise OCP, +1 headroom, "
+                         "ceil and nearest scale rules; column-wise OCP and ceil")
         elif kind == "spike":
             seq = [S.spike_step(s, dev) for s in range(S.SPIKE_STEPS)]
             for name, w, m in (("most_recent_w1", 1, 0), ("max_window_w16_m1", 16, 1)):
@@ -177,7 +224,9 @@ class Workload:
             grouped("cast", [x], [F.E4M3], 16)
             self.name = f"single bf16 tensor of {n} elements, E4M3, max-window 16"
         self.step_bytes = sum(p.bytes for p in self.parts)
-        self.elements = None
+        # small launches cannot be fed from Python fast enough: those
+        # workloads are timed by replaying a CUDA graph of `graph_steps` steps
+        self.graph_steps = {"current": 100, "spike": 16}.get(kind, 0)
 
     def step(self, k, ev=None):
         for i, p in enumerate(self.parts):
@@ -373,6 +422,18 @@ def run_ours(args, rank: int, world: int):
 
     K = args.steps
     P = len(W.parts)
+    graph = None
+    if W.graph_steps:
+        G = W.graph_steps
+        K = max(G, (K // G) * G)
+        l_cap = F.launch_count()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for k in range(G):
+                W.step(warm + k)
+        launches_per_graph = F.launch_count() - l_cap
+        graph.replay()
+        torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(P + 1)] for _ in range(K)]
     if world > 1:
         dist.barrier()
@@ -381,12 +442,18 @@ def run_ours(args, rank: int, world: int):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record()
-    for k in range(K):
-        W.step(warm + k, evs[k])
+    if graph is not None:
+        for _ in range(K // W.graph_steps):
+            graph.replay()
+    else:
+        for k in range(K):
+            W.step(warm + k, evs[k])
     t_end.record()
     torch.cuda.synchronize()
     host_t1 = time.time()
     launches = F.launch_count() - l0
+    if graph is not None:
+        launches = launches_per_graph * (K // W.graph_steps)
     clk = clocks.stop(host_t0, host_t1)
     if world > 1:
         dist.barrier()
@@ -397,14 +464,31 @@ def run_ours(args, rank: int, world: int):
 
     parts = {}
     for i, p in enumerate(W.parts):
-        pm = statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+        if graph is None:
+            ts = sorted(e[i].elapsed_time(e[i + 1]) for e in evs)
+            pm = statistics.mean(ts)
+            pct = {"p10": round(ts[len(ts) // 10], 5), "p50": round(ts[len(ts) // 2], 5),
+                   "p90": round(ts[(9 * len(ts)) // 10], 5)}
+        else:                       # graph replay: the step time split by bytes
+            pm = ms_step * p.bytes / W.step_bytes
+            pct = {"timing": f"CUDA-graph replay of {W.graph_steps} steps; step time split by bytes"}
         gbs = p.bytes / (pm * 1e-3) / 1e9
         parts[p.name] = {"kernel": p.kernel, "ms": round(pm, 5), "bytes": p.bytes,
-                         "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+                         "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4), **pct}
     dom = max(W.parts, key=lambda p: parts[p.name]["ms"])
     dpart = parts[dom.name]
 
-    e2e = None if args.no_e2e else run_e2e(W, args.e2e_steps, world, dev, warm + K)
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(W, args.e2e_steps, world, dev, warm + K)
+        if hasattr(torch._C, "_host_emptyCache"):
+            torch._C._host_emptyCache()          # give the staging mirrors back
+        if args.workload in ("decoder", "grad", "mx", "single"):
+            zc = run_e2e_zero_copy(args, world, dev)
+            e2e["staged_copy"] = {k: e2e[k] for k in ("value", "ms_per_step", "phases_ms", "path")}
+            e2e["zero_copy"] = zc
+            if zc["value"] > e2e["value"]:
+                e2e.update(value=zc["value"], ms_per_step=zc["ms_per_step"], path=zc["path"])
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -432,7 +516,9 @@ def run_ours(args, rank: int, world: int):
                          "peak": peak, "unit": "GB/s", "frac": dpart["frac"],
                          "peak_source": "measured: MEASURED_PEAKS.json hbm_gbs (copy)"
                          if peak_kind == "measured" else "fallback",
-                         "bytes_per_launch": dom.bytes, "traffic": None},
+                         "bytes_per_launch": dom.bytes,
+                         "traffic": captured_traffic() if (args.workload == "decoder"
+                                                           and dom.kernel == "cast_group_kernel") else None},
             "parts": parts,
             "gpu_launches": launches,
             "clocks": clk,
@@ -442,6 +528,31 @@ def run_ours(args, rank: int, world: int):
         if args.workload == "current":
             line["latency_us_per_cast"] = round(ms_step * 1e3, 2)
         print(json.dumps(line), flush=True)
+
+
+def run_e2e_zero_copy(args, world: int, dev):
+    """The same step with inputs and outputs in pinned host memory passed
+    straight to the C ABI: the kernels read the inputs and write the
+    results over NVLink-C2C, so each step moves the same host bytes."""
+    import torch
+    W = Workload(args.workload, args.n, dev, host_io=True)
+    for k in range(3):
+        W.step(k)
+    torch.cuda.synchronize()
+    steps = max(2, args.e2e_steps)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for k in range(steps):
+        W.step(3 + k)
+    b.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    for p in W.handles:
+        if hasattr(p, "close"):
+            p.close()
+    return {"value": round(world * W.step_bytes / (ms / steps * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms / steps, 3), "steps": steps,
+            "path": "pinned host buffers passed to the fp8q C ABI; kernels read and write them over NVLink-C2C (zero-copy)"}
 
 
 def run_e2e(W, steps: int, world: int, dev, k0: int):
@@ -470,29 +581,43 @@ def run_e2e(W, steps: int, world: int, dev, k0: int):
     h2d = sum(t.numel() * t.element_size() for t in ins0)
     d2h = sum(t.numel() * t.element_size() for t in outs0)
 
-    def one(k):
+    def one(k, ev=None):
         ins, outs = io(k)
+        if ev is not None:
+            ev[0].record()
         for t in ins:
             t.copy_(host_of(t), non_blocking=True)
+        if ev is not None:
+            ev[1].record()
         W.step(k)
+        if ev is not None:
+            ev[2].record()
         for t in outs:
             host_of(t).copy_(t, non_blocking=True)
+        if ev is not None:
+            ev[3].record()
 
     for k in range(k0, k0 + 2):
         one(k)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
     for k in range(steps):
-        one(k0 + 2 + k)
+        one(k0 + 2 + k, evs[k])
     b.record()
     torch.cuda.synchronize()
     ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    phase = [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i in range(3)]
     return {"value": round(world * W.step_bytes / (ms / steps * 1e-3) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(ms / steps, 3), "steps": steps,
+            "phases_ms": {"h2d": round(phase[0], 3), "casts": round(phase[1], 3),
+                          "d2h": round(phase[2], 3)},
+            "h2d_GBps": round(h2d / (phase[0] * 1e-3) / 1e9, 1) if phase[0] > 0 else None,
+            "d2h_GBps": round(d2h / (phase[2] * 1e-3) / 1e9, 1) if phase[2] > 0 else None,
             "path": "pinned host -> cudaMemcpyAsync -> fp8q C ABI -> cudaMemcpyAsync -> pinned host"}
 
 

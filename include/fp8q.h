@@ -106,6 +106,38 @@ typedef struct fp8q_state* fp8q_handle;
 FP8Q_API int fp8q_create(int format, int window, int margin_bits, int hysteresis_bits,
                          fp8q_handle* out);
 
+/* Estimators of the statistic the scale comes from (gist.science summary of
+ * "Max-Window Scale Estimation ...", Methodology, "Amax algorithms"):
+ *   FP8Q_EST_MAX_WINDOW  the largest amax of the last `window` casts (window 1
+ *                        is the most-recent rule, window 0 current scaling)
+ *   FP8Q_EST_SMOOTHED    a running average of the amax ("exponential
+ *                        smoothing", coefficient not given by the pages):
+ *                        avg <- avg + alpha * (amax - avg) in fp32 (three
+ *                        roundings, no FMA), started at the first cast's amax;
+ *                        a non-finite amax does not enter the average. */
+enum { FP8Q_EST_MAX_WINDOW = 0, FP8Q_EST_SMOOTHED = 1 };
+
+/* fp8q_create with a choice of estimator and a recompute interval
+ * ("Practice c06/E3" worked solution: recompute the scale every fixed number
+ * of steps).
+ *   estimator  FP8Q_EST_MAX_WINDOW or FP8Q_EST_SMOOTHED
+ *   alpha      smoothing coefficient in (0, 1] (used by FP8Q_EST_SMOOTHED)
+ *   interval   >= 1: the exponent is recomputed only when the number of
+ *              earlier casts is a multiple of interval, and kept otherwise
+ * With FP8Q_EST_SMOOTHED the window only sizes the history that
+ * fp8q_amax_history reports; the first cast uses current scaling. */
+FP8Q_API int fp8q_create_ex(int format, int window, int margin_bits, int hysteresis_bits,
+                            int estimator, float alpha, int interval, fp8q_handle* out);
+
+/* Read / restore the estimator state that fp8q_set_history does not cover:
+ * the running average (valid when *has_average) and the number of casts
+ * done (the phase of the recompute interval).  Both block until the
+ * handle's last cast has finished. */
+FP8Q_API int fp8q_get_estimator_state(fp8q_handle h, float* average, int* has_average,
+                                      long long* steps);
+FP8Q_API int fp8q_set_estimator_state(fp8q_handle h, float average, int has_average,
+                                      long long steps);
+
 /* Free a handle's device and host state.  Waits for the handle's last cast.
  * NULL is accepted (returns FP8Q_OK). */
 FP8Q_API int fp8q_destroy(fp8q_handle h);
@@ -147,6 +179,28 @@ FP8Q_API int fp8q_cast_multi(const fp8q_handle* hs, const void* const* xs, const
 FP8Q_API int mx_cast(const void* x, int dtype, int64_t rows, int64_t cols, int format,
                      int headroom_bits, uint8_t* q, uint8_t* e8m0,
                      unsigned long long* d_clipped, void* stream);
+
+/* MX scale-rounding rules and block directions for mx_cast_ex.  The pages
+ * ("what actually breaks low precision training", "The part I would rather
+ * not write") name the OCP floor rule, NVIDIA's MXFP8 recipe that rounds the
+ * shared scale up, and a comparison of floor, ceil and nearest rounding.
+ *   FP8Q_MX_FLOOR    E = floor(log2 A) - emax_elem (the OCP formula)
+ *   FP8Q_MX_CEIL     the smallest E with A * 2^-E <= fmax (never clips the block max)
+ *   FP8Q_MX_NEAREST  the integer E nearest to log2(A / fmax)
+ *   FP8Q_MX_ROWWISE  blocks of 32 consecutive elements of a row; e8m0 [rows, cols/32]
+ *   FP8Q_MX_COLWISE  blocks of 32 consecutive rows of a column; e8m0 [rows/32, cols] */
+enum { FP8Q_MX_FLOOR = 0, FP8Q_MX_CEIL = 1, FP8Q_MX_NEAREST = 2 };
+enum { FP8Q_MX_ROWWISE = 0, FP8Q_MX_COLWISE = 1 };
+
+/* MX cast with a choice of rule and block direction (mx_cast is the
+ * FP8Q_MX_FLOOR / FP8Q_MX_ROWWISE case).  E += headroom_bits (0..4), then
+ * clamped to [-127, 127].  q is row-major [rows, cols] in both directions.
+ *   rowwise: cols a multiple of 32.
+ *   colwise: rows a multiple of 32, cols a multiple of 16.
+ * One kernel launch (plus a memset of d_clipped). */
+FP8Q_API int mx_cast_ex(const void* x, int dtype, int64_t rows, int64_t cols, int format,
+                        int rule, int headroom_bits, int axis, uint8_t* q, uint8_t* e8m0,
+                        unsigned long long* d_clipped, void* stream);
 
 /* Read a handle's amax history (oldest first) to host memory.  Blocks until
  * the handle's last cast has finished.  capacity must be >= the window;
@@ -208,6 +262,13 @@ FP8Q_API int mx_error_stats(const void* x, int dtype, int64_t rows, int64_t cols
 FP8Q_API int fp8q_error_stats_noalloc(const void* x, int dtype, int64_t n, const uint8_t* q,
                                       int format, const float* d_scale_inv, double* d_out,
                                       void* stream);
+
+/* Number of pipeline waits on the current device that ran out of time since
+ * the last call (and reset it).  Kernels that stage tiles through TMA
+ * (column-wise mx_cast_ex) bound every wait for a tile; on timeout they count
+ * it here and stop instead of hanging, leaving their outputs incomplete.  A
+ * healthy run reads 0.  Synchronous. */
+FP8Q_API int fp8q_pipeline_status(unsigned int* timed_out_waits);
 
 /* Name of a status code (static string). */
 FP8Q_API const char* fp8q_strerror(int code);

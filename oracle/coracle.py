@@ -59,6 +59,10 @@ def lib():
         L.orc_mx_exp.restype = c_int
         L.orc_mx_cast.argtypes = [c_p, c_int, c_i64, c_i64, c_int, c_int, c_p, c_p, c_int]
         L.orc_mx_cast.restype = c_i64
+        L.orc_mx_exp_rule.argtypes = [c_u32, c_int, c_int, c_int]
+        L.orc_mx_exp_rule.restype = c_int
+        L.orc_mx_cast_ex.argtypes = [c_p, c_int, c_i64, c_i64, c_int, c_int, c_int, c_int, c_p, c_p, c_int]
+        L.orc_mx_cast_ex.restype = c_i64
         L.orc_stats.argtypes = [c_p, c_int, c_i64, c_p, c_int, c_int, c_p, c_int]
         L.orc_stats.restype = None
         L.orc_mx_stats.argtypes = [c_p, c_int, c_i64, c_i64, c_p, c_p, c_int, c_p, c_int]
@@ -156,3 +160,24 @@ def mx_stats(x: np.ndarray, q: np.ndarray, e8: np.ndarray, fmt: int, nthreads: i
     lib().orc_mx_stats(_ptr(x), _dtype_of(x), rows, cols, _ptr(np.ascontiguousarray(q)),
                        _ptr(np.ascontiguousarray(e8)), fmt, _ptr(out), nthreads)
     return float(out[0]), float(out[1]), int(out[2])
+
+
+MX_FLOOR, MX_CEIL, MX_NEAREST = 0, 1, 2
+ROWWISE, COLWISE = 0, 1
+
+
+def mx_exp_rule(amax_bits: int, fmt: int, rule: int, headroom: int) -> int:
+    return int(lib().orc_mx_exp_rule(amax_bits, fmt, rule, headroom))
+
+
+def mx_cast_ex(x: np.ndarray, fmt: int, rule: int, headroom: int, axis: int, nthreads: int = 1):
+    """x: [rows, cols] raw bits.  axis 0: e8m0 [rows, cols/32]; axis 1:
+    e8m0 [rows/32, cols].  Returns (q [rows, cols], e8m0, clipped)."""
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), dtype=np.uint8)
+    e8 = np.empty((rows, cols // 32) if axis == 0 else (rows // 32, cols), dtype=np.uint8)
+    clipped = lib().orc_mx_cast_ex(_ptr(x), _dtype_of(x), rows, cols, fmt, rule, headroom, axis,
+                                   _ptr(q), _ptr(e8), nthreads)
+    return q, e8, int(clipped)
+

@@ -388,3 +388,82 @@ void orc_mx_stats(const void* x, int dtype, int64_t rows, int64_t cols, const ui
     out[1] = cnt ? sm / (double)cnt : 0.0;
     out[2] = (double)cnt;
 }
+
+/* --------------------------------------------------------------------------
+ * MX scale-rounding rules and block direction.
+ *
+ * "what actually breaks low precision training" ("The part I would rather not
+ * write"): NVIDIA's MXFP8 pre-training recipe rounds the shared scale up
+ * instead of using the specification's floor, and a 2025 study compares
+ * floor, ceil and nearest rounding of the scale.  Readings adopted:
+ *   rule 0  OCP floor: E = floor(log2 A) - emax_elem
+ *   rule 1  ceil: the smallest integer E with A * 2^-E <= fmax (the scaled
+ *           block max never exceeds the format maximum)
+ *   rule 2  nearest: the integer E nearest to log2(A / fmax) (no ties: the
+ *           half-way point would need A / fmax = 2^k * sqrt 2)
+ * then E += headroom and E is clamped to [-127, 127]; a zero block gets -127.
+ * axis 0: blocks of 32 consecutive elements of a row (e8m0 [rows, cols/32]);
+ * axis 1: blocks of 32 consecutive rows of a column (e8m0 [rows/32, cols]).
+ * ------------------------------------------------------------------------ */
+int orc_mx_exp_rule(uint32_t amax_bits, int fmt, int rule, int headroom) {
+    if (rule == 0) return orc_mx_exp(amax_bits, fmt, headroom);
+    mf_t f = mf_of(fmt);
+    uint32_t a = amax_bits & 0x7FFFFFFFu;
+    if (a == 0) return -127;
+    float af;
+    memcpy(&af, &a, 4);
+    double A = (double)af;
+    double fmax = orc_decode(fmt, f.maxcode);
+    int E0 = -400;                       /* smallest E with A * 2^-E <= fmax */
+    for (int e = -200; e <= 200; e++)
+        if (ldexp(A, -e) <= fmax) { E0 = e; break; }
+    int E = E0;
+    if (rule == 2) {
+        /* E0 puts the scaled max in (fmax/2, fmax], E0 - 1 in (fmax, 2 fmax];
+         * keep E0 when its log distance is the smaller one:
+         * fmax / (A 2^-E0) <= (A 2^-(E0-1)) / fmax  <=>  fmax^2 2^(2 E0 - 1) <= A^2
+         * (both sides exact in double: 18- and 48-bit significands). */
+        if (!(fmax * fmax * ldexp(1.0, 2 * E0 - 1) <= A * A)) E = E0 - 1;
+    }
+    E += headroom;
+    if (E < -127) E = -127;
+    if (E > 127) E = 127;
+    return E;
+}
+
+int64_t orc_mx_cast_ex(const void* x, int dtype, int64_t rows, int64_t cols, int fmt, int rule,
+                       int headroom, int axis, uint8_t* q, uint8_t* e8m0, int nthreads) {
+    mf_t f = mf_of(fmt);
+    int64_t nblocks = rows * cols / 32;
+    int64_t clipped = 0;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(static, 2048) reduction(+ : clipped)
+    for (int64_t b = 0; b < nblocks; b++) {
+        /* element j of block b sits at idx(b, j) */
+        int64_t r0, c0, step;
+        if (axis == 0) { r0 = b / (cols / 32); c0 = (b % (cols / 32)) * 32; step = 1; }
+        else { r0 = (b / cols) * 32; c0 = b % cols; step = cols; }
+        int64_t base = r0 * cols + c0;
+        uint32_t amax = 0;
+        for (int j = 0; j < 32; j++) {
+            uint32_t a = load_bits(x, dtype, base + j * step) & 0x7FFFFFFFu;
+            if (a > amax) amax = a;
+        }
+        if (amax >= 0x7F800000u) {
+            e8m0[b] = 0xFF;
+            for (int j = 0; j < 32; j++)
+                q[base + j * step] =
+                    (uint8_t)(((load_bits(x, dtype, base + j * step) >> 31) << 7) | 0x7Fu);
+            continue;
+        }
+        int E = orc_mx_exp_rule(amax, fmt, rule, headroom);
+        e8m0[b] = (uint8_t)(E + 127);
+        for (int j = 0; j < 32; j++) {
+            int cl;
+            q[base + j * step] = (uint8_t)cast_f32_bits(&f, load_bits(x, dtype, base + j * step), -E, &cl);
+            clipped += cl;
+        }
+    }
+    return clipped;
+}
+

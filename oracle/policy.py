@@ -10,6 +10,16 @@ The gist.science summary of "Max-Window Scale Estimation for Near-Lossless HiF8
 W8A8 QAT" (Methodology, "Amax algorithms") names the variants: most-recent
 (window 1), max over a history window (64 there), and current tensor scaling.
 
+Estimators ("Amax algorithms" of the summary; "recompute the scale every
+fixed number of steps" of the worked solution):
+  * max-window (default): the statistic is the largest amax of the window;
+  * exponential smoothing: the statistic is a running average of the amax,
+    avg <- avg + alpha * (amax - avg) evaluated in fp32 (three roundings, no
+    fused multiply-add), started at the first cast's amax; a non-finite amax
+    does not enter the average;
+  * recompute interval k: the exponent is recomputed only when the number
+    of earlier casts is a multiple of k, and kept otherwise.
+
 Readings adopted where the pages are silent:
   * the window holds the amaxes of the W steps *before* this one; this step's
     amax enters it after the cast;
@@ -40,19 +50,36 @@ def bits_of_f32(v: float) -> int:
     return struct.unpack("<I", struct.pack("<f", v))[0]
 
 
+MAX_WINDOW, EMA = 0, 1
+
+
 class ScalingState:
     """One tensor's history ring, previous exponent and policy."""
 
-    def __init__(self, fmt: int, window: int, margin: int = 0, hysteresis: int = 0):
+    def __init__(self, fmt: int, window: int, margin: int = 0, hysteresis: int = 0,
+                 estimator: int = MAX_WINDOW, alpha: float = 1.0, interval: int = 1):
         self.fmt, self.window, self.margin, self.hysteresis = fmt, window, margin, hysteresis
+        self.estimator, self.interval = estimator, interval
+        self.alpha = np.float32(alpha)
         self.hist: list[int] = []          # amax bit patterns, oldest first
         self.prev_e: int | None = None
         self.steps = 0
+        self.avg: np.float32 | None = None   # running average (smoothing estimator)
 
     def uses_current(self) -> bool:
+        if self.estimator == EMA:
+            return self.steps == 0
         return self.window == 0 or not self.hist
 
+    def statistic(self) -> int:
+        """fp32 bits of the statistic the next exponent comes from."""
+        if self.estimator == EMA:
+            return 0x7FC00000 if self.avg is None else bits_of_f32(float(self.avg))
+        return max(self.hist)
+
     def exponent(self, window_amax_bits: int) -> int:
+        if (self.interval > 1 and self.prev_e is not None and self.steps % self.interval != 0):
+            return self.prev_e
         e_new = coracle.scale_exp(window_amax_bits, self.fmt, self.margin)
         if e_new is None:                               # zero or non-finite
             return self.prev_e if self.prev_e is not None else 0
@@ -67,13 +94,19 @@ class ScalingState:
         if self.uses_current():
             a_w = coracle.amax(x, nthreads)
         else:
-            a_w = max(self.hist)
+            a_w = self.statistic()
         e = self.exponent(a_w)
         q, a_cur, clipped = coracle.cast(x, self.fmt, e, nthreads)
         self.record(a_cur, e)
         return q, a_cur, bits_of_f32(2.0 ** -e), clipped, e
 
     def record(self, amax_bits: int, e: int):
+        if self.estimator == EMA and (amax_bits & 0x7FFFFFFF) < 0x7F800000:
+            a = np.float32(f32_of_bits(amax_bits))
+            if self.avg is None:
+                self.avg = a
+            else:
+                self.avg = np.float32(self.avg + np.float32(self.alpha * np.float32(a - self.avg)))
         if self.window > 0:
             self.hist.append(amax_bits)
             del self.hist[:-self.window]

@@ -329,3 +329,53 @@ def error_stats(fmt, vals, codes, scale_of_index):
     if k == 0:
         return Fraction(0), Fraction(0), 0
     return sq / k, sm / k, k
+
+
+# ---------------------------------------------------------------------------
+# MX scale-rounding rules and block direction (see oracle.c for the readings:
+# 0 OCP floor, 1 smallest E with A 2^-E <= fmax, 2 E nearest log2(A / fmax))
+# ---------------------------------------------------------------------------
+
+def mx_exp_rule(fmt: Minifloat, amax: Fraction, rule: int, headroom: int) -> int:
+    if rule == 0:
+        return mx_exp(fmt, amax, headroom)
+    if amax == 0:
+        return -127
+    fmax = fmax_of(fmt)
+    e = -200
+    while amax / Fraction(2) ** e > fmax:
+        e += 1
+    if rule == 2:
+        # keep e when fmax / (A 2^-e) <= (A 2^-(e-1)) / fmax, else e - 1
+        lo = fmax / (amax / Fraction(2) ** e)
+        hi = (amax / Fraction(2) ** (e - 1)) / fmax
+        if not lo <= hi:
+            e -= 1
+    return max(-127, min(127, e + headroom))
+
+
+def mx_cast_tensor_ex(fmt, vals, rows, cols, rule, headroom, axis):
+    """vals row-major [rows, cols]; returns (q list row-major, e8m0 list in
+    its own row-major layout, clipped)."""
+    q = [None] * (rows * cols)
+    if axis == 0:
+        blocks = [[r * cols + c0 + j for j in range(32)] for r in range(rows) for c0 in range(0, cols, 32)]
+    else:
+        blocks = [[(r0 + j) * cols + c for j in range(32)] for r0 in range(0, rows, 32) for c in range(cols)]
+    e8, clipped = [], 0
+    for idx in blocks:
+        blk = [vals[i] for i in idx]
+        a = tensor_amax(blk)
+        if a in (NAN, INF):
+            e8.append(0xFF)
+            for i, (s, _) in zip(idx, blk):
+                q[i] = fmt.sign_bit * s | nan_code(fmt)
+            continue
+        E = mx_exp_rule(fmt, a, rule, headroom)
+        e8.append(E + 127)
+        for i, (s, m) in zip(idx, blk):
+            c, cl = cast(fmt, s, m, -E)
+            q[i] = c
+            clipped += int(cl)
+    return q, e8, clipped
+

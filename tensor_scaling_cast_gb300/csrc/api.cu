@@ -56,6 +56,9 @@ static const uint32_t kMagic = 0xF8A5C0DEu;
 struct fp8q_state {
   uint32_t magic;
   int format, window, margin, hyst;
+  int estimator, interval;
+  float alpha;
+  long long host_casts;     // casts enqueued, mirrored on the host
   int device;
   DevState* dev;
   int host_count;           // valid history entries, mirrored on the host
@@ -108,23 +111,35 @@ FP8Q_API const char* fp8q_strerror(int code) {
 
 FP8Q_API const char* fp8q_last_cuda_error(void) { return g_cuda_err; }
 
+FP8Q_API int fp8q_pipeline_status(unsigned int* timed_out_waits) {
+  if (!timed_out_waits) return FP8Q_EINVAL;
+  cudaError_t e = read_wait_timeouts(timed_out_waits);
+  return e == cudaSuccess ? FP8Q_OK : fail_cuda(e);
+}
+
 FP8Q_API long long fp8q_launch_count(void) { return g_launches.load(); }
 
-FP8Q_API int fp8q_create(int format, int window, int margin_bits, int hysteresis_bits,
-                         fp8q_handle* out) {
+FP8Q_API int fp8q_create_ex(int format, int window, int margin_bits, int hysteresis_bits,
+                            int estimator, float alpha, int interval, fp8q_handle* out) {
   if (!out) return FP8Q_EINVAL;
   *out = nullptr;
   if (!format_ok(format)) return FP8Q_EDTYPE;
   if (window < 0 || window > FP8Q_MAX_WINDOW || margin_bits < 0 || margin_bits > 16 ||
       hysteresis_bits < 0 || hysteresis_bits > 16)
     return FP8Q_EINVAL;
+  if (estimator != FP8Q_EST_MAX_WINDOW && estimator != FP8Q_EST_SMOOTHED) return FP8Q_EINVAL;
+  if (!(alpha > 0.0f && alpha <= 1.0f) || interval < 1) return FP8Q_EINVAL;
   fp8q_state* h = new (std::nothrow) fp8q_state();
   if (!h) return FP8Q_ENOMEM;
   h->format = format;
   h->window = window;
   h->margin = margin_bits;
   h->hyst = hysteresis_bits;
+  h->estimator = estimator;
+  h->alpha = alpha;
+  h->interval = interval;
   h->host_count = 0;
+  h->host_casts = 0;
   h->has_last = false;
   cudaError_t e = cudaGetDevice(&h->device);
   if (e != cudaSuccess) { delete h; return fail_cuda(e); }
@@ -136,12 +151,21 @@ FP8Q_API int fp8q_create(int format, int window, int margin_bits, int hysteresis
   init.window = window;
   init.margin = margin_bits;
   init.hyst = hysteresis_bits;
+  init.estimator = estimator;
+  init.alpha = alpha;
+  init.interval = interval;
   e = cudaMemcpy(h->dev, &init, sizeof init, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->last, cudaEventDisableTiming);
   if (e != cudaSuccess) { cudaFree(h->dev); delete h; return fail_cuda(e); }
   h->magic = kMagic;
   *out = h;
   return FP8Q_OK;
+}
+
+FP8Q_API int fp8q_create(int format, int window, int margin_bits, int hysteresis_bits,
+                         fp8q_handle* out) {
+  return fp8q_create_ex(format, window, margin_bits, hysteresis_bits, FP8Q_EST_MAX_WINDOW, 1.0f,
+                        1, out);
 }
 
 FP8Q_API int fp8q_destroy(fp8q_handle h) {
@@ -176,7 +200,9 @@ static int plan_and_launch(const fp8q_handle* hs, const void* const* xs, const i
       const int64_t ce = chunk_elems(dt);
       const long long nch = std::max<long long>(1, (n + ce - 1) / ce);
       int mode = kDelayed;
-      if (h->window == 0 || h->host_count == 0) mode = (n <= ce) ? kCurrentLocal : kCurrentPre;
+      const bool current = h->estimator == FP8Q_EST_SMOOTHED ? h->host_casts == 0
+                                                             : (h->window == 0 || h->host_count == 0);
+      if (current) mode = (n <= ce) ? kCurrentLocal : kCurrentPre;
       TensorDesc d;
       d.x = xs[base + i];
       d.q = qs[base + i];
@@ -215,6 +241,7 @@ static int plan_and_launch(const fp8q_handle* hs, const void* const* xs, const i
     for (int i = 0; i < m; ++i) {
       fp8q_handle h = hs[base + i];
       if (h->window > 0 && h->host_count < h->window) h->host_count++;
+      h->host_casts++;
       int st = record_last(h, s);
       if (st != FP8Q_OK) return st;
     }
@@ -260,12 +287,15 @@ FP8Q_API int fp8q_cast_multi(const fp8q_handle* hs, const void* const* xs, const
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
-FP8Q_API int mx_cast(const void* x, int dtype, int64_t rows, int64_t cols, int format,
-                     int headroom_bits, uint8_t* q, uint8_t* e8m0,
-                     unsigned long long* d_clipped, void* stream) {
+FP8Q_API int mx_cast_ex(const void* x, int dtype, int64_t rows, int64_t cols, int format,
+                        int rule, int headroom_bits, int axis, uint8_t* q, uint8_t* e8m0,
+                        unsigned long long* d_clipped, void* stream) {
   if (!dtype_ok(dtype) || !format_ok(format)) return FP8Q_EDTYPE;
-  if (rows < 0 || cols <= 0 || cols % 32 != 0 || headroom_bits < 0 || headroom_bits > 4)
-    return FP8Q_EINVAL;
+  if (rule < FP8Q_MX_FLOOR || rule > FP8Q_MX_NEAREST) return FP8Q_EINVAL;
+  if (axis != FP8Q_MX_ROWWISE && axis != FP8Q_MX_COLWISE) return FP8Q_EINVAL;
+  if (rows < 0 || cols <= 0 || headroom_bits < 0 || headroom_bits > 4) return FP8Q_EINVAL;
+  if (axis == FP8Q_MX_ROWWISE && cols % 32 != 0) return FP8Q_EINVAL;
+  if (axis == FP8Q_MX_COLWISE && (rows % 32 != 0 || cols % 16 != 0)) return FP8Q_EINVAL;
   if (rows > 0 && cols > (int64_t(1) << 46) / rows) return FP8Q_EINVAL;
   const int64_t n = rows * cols;
   if (n > 0 && (!x || !q || !e8m0)) return FP8Q_EINVAL;
@@ -277,9 +307,19 @@ FP8Q_API int mx_cast(const void* x, int dtype, int64_t rows, int64_t cols, int f
   }
   if (n == 0) return FP8Q_OK;
   int launches = 0;
-  cudaError_t e = launch_mx(x, dtype, n, format, headroom_bits, q, e8m0, d_clipped, s, &launches);
+  cudaError_t e = axis == FP8Q_MX_ROWWISE
+                      ? launch_mx(x, dtype, n, format, headroom_bits, rule, q, e8m0, d_clipped, s, &launches)
+                      : launch_mx_colwise(x, dtype, rows, cols, format, headroom_bits, rule, q, e8m0,
+                                          d_clipped, s, &launches);
   g_launches += launches;
   return e == cudaSuccess ? FP8Q_OK : fail_cuda(e);
+}
+
+FP8Q_API int mx_cast(const void* x, int dtype, int64_t rows, int64_t cols, int format,
+                     int headroom_bits, uint8_t* q, uint8_t* e8m0,
+                     unsigned long long* d_clipped, void* stream) {
+  return mx_cast_ex(x, dtype, rows, cols, format, FP8Q_MX_FLOOR, headroom_bits, FP8Q_MX_ROWWISE,
+                    q, e8m0, d_clipped, stream);
 }
 
 FP8Q_API int fp8q_amax_history(fp8q_handle h, float* host_out, int capacity, int* n_valid) {
@@ -324,6 +364,9 @@ static int write_state(fp8q_handle h, const float* host_in, int n, int prev_exp,
   d.window = h->window;
   d.margin = h->margin;
   d.hyst = h->hyst;
+  d.estimator = h->estimator;
+  d.alpha = h->alpha;
+  d.interval = h->interval;
   for (int i = 0; i < n; ++i) {
     uint32_t b;
     std::memcpy(&b, &host_in[i], 4);
@@ -335,9 +378,46 @@ static int write_state(fp8q_handle h, const float* host_in, int n, int prev_exp,
   d.has_prev = prev_exp != FP8Q_NO_EXP;
   d.prev_e = d.has_prev ? prev_exp : 0;
   d.steps = steps;
+  d.phase = (int32_t)(steps % h->interval);
   cudaError_t e = cudaMemcpy(h->dev, &d, sizeof d, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return fail_cuda(e);
   h->host_count = n;
+  h->host_casts = steps;
+  return FP8Q_OK;
+}
+
+FP8Q_API int fp8q_get_estimator_state(fp8q_handle h, float* average, int* has_average,
+                                      long long* steps) {
+  if (!handle_ok(h)) return FP8Q_EHANDLE;
+  int st = check_device(h);
+  if (st == FP8Q_OK) st = wait_last(h);
+  if (st != FP8Q_OK) return st;
+  DevState d;
+  cudaError_t e = cudaMemcpy(&d, h->dev, sizeof d, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (average) *average = d.avg;
+  if (has_average) *has_average = d.has_avg;
+  if (steps) *steps = d.steps;
+  return FP8Q_OK;
+}
+
+FP8Q_API int fp8q_set_estimator_state(fp8q_handle h, float average, int has_average,
+                                      long long steps) {
+  if (!handle_ok(h)) return FP8Q_EHANDLE;
+  if (steps < 0) return FP8Q_EINVAL;
+  int st = check_device(h);
+  if (st == FP8Q_OK) st = wait_last(h);
+  if (st != FP8Q_OK) return st;
+  DevState d;
+  cudaError_t e = cudaMemcpy(&d, h->dev, sizeof d, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e);
+  d.avg = average;
+  d.has_avg = has_average ? 1 : 0;
+  d.steps = steps;
+  d.phase = (int32_t)(steps % h->interval);
+  e = cudaMemcpy(h->dev, &d, sizeof d, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fail_cuda(e);
+  h->host_casts = steps;
   return FP8Q_OK;
 }
 

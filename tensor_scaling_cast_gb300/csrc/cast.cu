@@ -40,11 +40,10 @@ template <int DT, bool FULL>
 __device__ __forceinline__ void load_chunk(const char* x, int64_t rem, uint4 (&r)[kUnroll]) {
   constexpr int EPL = Tr<DT>::EPL;
   const uint4* px = reinterpret_cast<const uint4*>(x) + threadIdx.x;
-  if (FULL) {
+  if constexpr (FULL) {
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) r[u] = __ldcs(px + u * kThreads);
-    return;
-  }
+  } else {
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u) {
     const int64_t e0 = (int64_t)(u * kThreads + threadIdx.x) * EPL;
@@ -64,6 +63,7 @@ __device__ __forceinline__ void load_chunk(const char* x, int64_t rem, uint4 (&r
       }
       r[u] = make_uint4(w[0], w[1], w[2], w[3]);
     }
+  }
   }
 }
 
@@ -124,9 +124,31 @@ __device__ __forceinline__ uint32_t window_max(const DevState* st) {
   return __reduce_max_sync(0xFFFFFFFFu, a);
 }
 
+// Exponent of this cast.  With a recompute interval k > 1 the previous
+// exponent is kept unless the number of earlier casts is a multiple of k
+// (phase = casts mod k, kept by the finishing CTA).
 __device__ __forceinline__ int state_exp(const DevState* st, uint32_t a_w) {
-  return pick_exp(a_w, __ldcg(&st->format), __ldcg(&st->margin), __ldcg(&st->hyst),
-                  __ldcg(&st->prev_e), __ldcg(&st->has_prev) != 0);
+  const int prev = __ldcg(&st->prev_e);
+  const bool has_prev = __ldcg(&st->has_prev) != 0;
+  if (has_prev && __ldcg(&st->phase) != 0) return prev;
+  return pick_exp(a_w, __ldcg(&st->format), __ldcg(&st->margin), __ldcg(&st->hyst), prev, has_prev);
+}
+
+// Statistic of the smoothed estimator: the running average, or NaN (keep
+// the previous exponent) while no finite amax has been seen.
+__device__ __forceinline__ uint32_t smoothed_stat(const DevState* st) {
+  return __ldcg(&st->has_avg) ? (__float_as_uint(__ldcg(&st->avg)) & 0x7FFFFFFFu) : 0x7FC00000u;
+}
+
+// Warp 0: the statistic of this cast (window maximum, running average or
+// current-scaling pre-pass amax) and the exponent, published in *s_e.
+__device__ __forceinline__ void warp_exp(const DevState* st, int mode, int* s_e) {
+  uint32_t a_w;
+  if (mode == kDelayed)
+    a_w = (__ldcg(&st->estimator) == FP8Q_EST_SMOOTHED) ? smoothed_stat(st) : window_max(st);
+  else
+    a_w = __ldcg(&st->pre_amax);
+  if (threadIdx.x == 0) *s_e = state_exp(st, a_w);
 }
 
 // Thread 0 of the CTA that completes the tensor: publish and advance state.
@@ -146,9 +168,16 @@ __device__ void finish_tensor(DevState* st, const GroupHeader& h, int t, int e) 
     st->head = (hd + 1 == W) ? 0 : hd + 1;
     if (st->count < W) st->count = st->count + 1;
   }
+  if (st->estimator == FP8Q_EST_SMOOTHED && a < 0x7F800000u) {
+    // avg <- avg + alpha * (amax - avg): three fp32 roundings, no FMA
+    const float af = __uint_as_float(a);
+    st->avg = st->has_avg ? __fadd_rn(st->avg, __fmul_rn(st->alpha, __fsub_rn(af, st->avg))) : af;
+    st->has_avg = 1;
+  }
   st->prev_e = e;
   st->has_prev = 1;
   st->steps = st->steps + 1;
+  st->phase = (st->phase + 1 >= st->interval) ? 0 : st->phase + 1;
   st->amax_acc = 0u;
   st->clip_acc = 0ull;
   st->pre_amax = 0u;
@@ -178,10 +207,7 @@ __device__ void cast_segment(const TensorDesc& d, int c0, int c1, int mode, int*
     e_out = e;
     return;
   }
-  if (threadIdx.x < 32) {
-    const uint32_t a_w = (mode == kDelayed) ? window_max(d.st) : __ldcg(&d.st->pre_amax);
-    if (threadIdx.x == 0) *s_e = state_exp(d.st, a_w);
-  }
+  if (threadIdx.x < 32) warp_exp(d.st, mode, s_e);
   __syncthreads();
   const int e = *s_e;
   const float s = pow2f(e);

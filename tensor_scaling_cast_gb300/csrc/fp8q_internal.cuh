@@ -26,7 +26,13 @@ struct __align__(256) DevState {
   int32_t prev_e;                   // exponent of the last cast
   int32_t has_prev;
   int32_t format, window, margin, hyst;
-  long long steps;
+  long long steps;                  // casts done
+  int32_t estimator;                // FP8Q_EST_MAX_WINDOW or FP8Q_EST_SMOOTHED
+  float alpha;                      // smoothing coefficient
+  int32_t interval;                 // recompute the exponent every `interval` casts
+  int32_t phase;                    // casts done, modulo interval
+  float avg;                        // running average of the amax (smoothed estimator)
+  int32_t has_avg;
 };
 
 enum Mode : int { kDelayed = 0, kCurrentPre = 1, kCurrentLocal = 2 };
@@ -66,12 +72,17 @@ cudaError_t launch_cast_group(const GroupHeader& h, const TensorDesc* d, int cou
                               cudaStream_t s, int* launches);
 cudaError_t launch_amax_group(const GroupHeader& h, const TensorDesc* d, int count,
                               cudaStream_t s, int* launches);
-cudaError_t launch_mx(const void* x, int dtype, int64_t nelem, int format, int headroom,
+cudaError_t launch_mx(const void* x, int dtype, int64_t nelem, int format, int headroom, int rule,
                       uint8_t* q, uint8_t* e8m0, unsigned long long* clipped, cudaStream_t s,
                       int* launches);
+cudaError_t launch_mx_colwise(const void* x, int dtype, int64_t rows, int64_t cols, int format,
+                              int headroom, int rule, uint8_t* q, uint8_t* e8m0,
+                              unsigned long long* clipped, cudaStream_t s, int* launches);
 cudaError_t launch_stats(const void* x, int dtype, int64_t n, const uint8_t* q, int format,
                          const float* scale_inv, const uint8_t* e8m0, double* out,
                          cudaStream_t s, int* launches);
+
+cudaError_t read_wait_timeouts(unsigned int* count);   // and reset to 0
 
 int sm_count(int device);
 int record_cuda_error(cudaError_t e);   // keeps the text, returns FP8Q_ECUDA

@@ -17,6 +17,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libfp8q.so")
 
 E4M3, E5M2 = 0, 1
+MX_FLOOR, MX_CEIL, MX_NEAREST = 0, 1, 2
+MX_ROWWISE, MX_COLWISE = 0, 1
+EST_MAX_WINDOW, EST_SMOOTHED = 0, 1
 F32, BF16 = 0, 1
 NO_EXP = -(2 ** 31)
 MAX_WINDOW = 256
@@ -46,10 +49,15 @@ def load() -> ctypes.CDLL:
     L = ctypes.CDLL(LIB_PATH)
     p, i, i64, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
     L.fp8q_create.argtypes = [i, i, i, i, ctypes.POINTER(p)]
+    L.fp8q_create_ex.argtypes = [i, i, i, i, i, f, i, ctypes.POINTER(p)]
+    L.fp8q_get_estimator_state.argtypes = [p, ctypes.POINTER(f), ctypes.POINTER(i),
+                                           ctypes.POINTER(ctypes.c_longlong)]
+    L.fp8q_set_estimator_state.argtypes = [p, f, i, ctypes.c_longlong]
     L.fp8q_destroy.argtypes = [p]
     L.fp8q_cast.argtypes = [p, p, i, i64, p, p, p, p, p]
     L.fp8q_cast_multi.argtypes = [p, p, p, p, p, p, p, p, i, p]
     L.mx_cast.argtypes = [p, i, i64, i64, i, i, p, p, p, p]
+    L.mx_cast_ex.argtypes = [p, i, i64, i64, i, i, i, i, p, p, p, p]
     L.fp8q_amax_history.argtypes = [p, ctypes.POINTER(f), i, ctypes.POINTER(i)]
     L.fp8q_scale_state.argtypes = [p, ctypes.POINTER(i), ctypes.POINTER(ctypes.c_longlong)]
     L.fp8q_set_history.argtypes = [p, ctypes.POINTER(f), i, i]
@@ -57,11 +65,14 @@ def load() -> ctypes.CDLL:
     L.fp8q_error_stats.argtypes = [p, i, i64, p, i, p, p, p]
     L.mx_error_stats.argtypes = [p, i, i64, i64, p, p, i, p, p]
     L.fp8q_error_stats_noalloc.argtypes = [p, i, i64, p, i, p, p, p]
+    L.fp8q_pipeline_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+    L.fp8q_pipeline_status.restype = i
     L.fp8q_strerror.argtypes = [i]
     L.fp8q_strerror.restype = ctypes.c_char_p
     L.fp8q_last_cuda_error.restype = ctypes.c_char_p
     L.fp8q_launch_count.restype = ctypes.c_longlong
-    for name in ("fp8q_create", "fp8q_destroy", "fp8q_cast", "fp8q_cast_multi", "mx_cast",
+    for name in ("fp8q_create", "fp8q_create_ex", "fp8q_get_estimator_state",
+                 "fp8q_set_estimator_state", "fp8q_destroy", "fp8q_cast", "fp8q_cast_multi", "mx_cast", "mx_cast_ex",
                  "fp8q_amax_history", "fp8q_scale_state", "fp8q_set_history", "fp8q_reset",
                  "fp8q_error_stats", "mx_error_stats", "fp8q_error_stats_noalloc"):
         getattr(L, name).restype = i
@@ -95,6 +106,13 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def fp8q_pipeline_status() -> int:
+    """Pipeline waits that timed out on the current device since the last call."""
+    n = ctypes.c_uint()
+    _check(load().fp8q_pipeline_status(ctypes.byref(n)), "fp8q_pipeline_status")
+    return n.value
+
+
 def launch_count() -> int:
     return int(load().fp8q_launch_count())
 
@@ -105,6 +123,28 @@ def fp8q_create(fmt: int, window: int, margin: int = 0, hysteresis: int = 0) -> 
     h = ctypes.c_void_p()
     _check(load().fp8q_create(fmt, window, margin, hysteresis, ctypes.byref(h)), "fp8q_create")
     return h.value
+
+
+def fp8q_create_ex(fmt: int, window: int, margin: int = 0, hysteresis: int = 0,
+                   estimator: int = EST_MAX_WINDOW, alpha: float = 1.0, interval: int = 1) -> int:
+    h = ctypes.c_void_p()
+    _check(load().fp8q_create_ex(fmt, window, margin, hysteresis, estimator, alpha, interval,
+                                 ctypes.byref(h)), "fp8q_create_ex")
+    return h.value
+
+
+def fp8q_get_estimator_state(h: int):
+    """(running average or None, number of casts)."""
+    a, ha, st = ctypes.c_float(), ctypes.c_int(), ctypes.c_longlong()
+    _check(load().fp8q_get_estimator_state(ctypes.c_void_p(h), ctypes.byref(a), ctypes.byref(ha),
+                                           ctypes.byref(st)), "fp8q_get_estimator_state")
+    return (a.value if ha.value else None), st.value
+
+
+def fp8q_set_estimator_state(h: int, average, steps: int):
+    _check(load().fp8q_set_estimator_state(ctypes.c_void_p(h), 0.0 if average is None else average,
+                                           0 if average is None else 1, steps),
+           "fp8q_set_estimator_state")
 
 
 def fp8q_destroy(h: int):
@@ -139,6 +179,14 @@ def mx_cast(x: torch.Tensor, fmt: int, headroom: int, q: torch.Tensor, e8m0: tor
     rows, cols = x.shape
     _check(load().mx_cast(_ptr(x), _dtype(x), rows, cols, fmt, headroom, _ptr(q), _ptr(e8m0),
                           _ptr(clipped), _stream(stream)), "mx_cast")
+
+
+def mx_cast_ex(x: torch.Tensor, fmt: int, rule: int, headroom: int, axis: int, q: torch.Tensor,
+               e8m0: torch.Tensor, clipped=None, stream=None):
+    """axis MX_ROWWISE: e8m0 [rows, cols/32]; MX_COLWISE: e8m0 [rows/32, cols]."""
+    rows, cols = x.shape
+    _check(load().mx_cast_ex(_ptr(x), _dtype(x), rows, cols, fmt, rule, headroom, axis, _ptr(q),
+                             _ptr(e8m0), _ptr(clipped), _stream(stream)), "mx_cast_ex")
 
 
 def fp8q_amax_history(h: int, capacity: int = MAX_WINDOW) -> list[float]:
@@ -197,9 +245,10 @@ class ScaledCast:
     """One tensor's scaling state on the GPU (owns an fp8q handle) with
     output buffers allocated by torch."""
 
-    def __init__(self, fmt: int, window: int, margin: int = 0, hysteresis: int = 0):
+    def __init__(self, fmt: int, window: int, margin: int = 0, hysteresis: int = 0,
+                 estimator: int = EST_MAX_WINDOW, alpha: float = 1.0, interval: int = 1):
         self.fmt, self.window, self.margin, self.hysteresis = fmt, window, margin, hysteresis
-        self.handle = fp8q_create(fmt, window, margin, hysteresis)
+        self.handle = fp8q_create_ex(fmt, window, margin, hysteresis, estimator, alpha, interval)
 
     def __call__(self, x: torch.Tensor, q: torch.Tensor | None = None, stream=None):
         """Returns (q uint8, scale_inv f32[1], amax f32[1], clipped i64[1]) on x's device."""

@@ -273,6 +273,68 @@ def test_mx_edge_values(fmt, dtype):
         assert int(cl.item()) == c_o
 
 
+def _mx_ex_gpu(x, fmt, rule, headroom, axis):
+    rows, cols = x.shape
+    q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+    e8 = torch.empty((rows, cols // 32) if axis == 0 else (rows // 32, cols), dtype=torch.uint8, device="cuda")
+    cl = torch.empty(1, dtype=torch.int64, device="cuda")
+    F.mx_cast_ex(x, fmt, rule, headroom, axis, q, e8, cl)
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), e8.cpu().numpy(), int(cl.item())
+
+
+@pytest.mark.parametrize("rule,axis", [(1, 0), (2, 0), (0, 1), (1, 1), (2, 1)])
+def test_mx_rules_and_axes_full_size(rule, axis):
+    """bf16 [16384, 8192] tanh(N(0,2)) -> MX E4M3 under the round-up (ceil)
+    and nearest scale rules, row-wise and column-wise 32-blocks."""
+    x = synthetic.mx_tanh("cuda")
+    xb = host_bits(x).reshape(x.shape)
+    q, e8, cl = _mx_ex_gpu(x, 0, rule, 0, axis)
+    q_o, e8_o, c_o = coracle.mx_cast_ex(xb, 0, rule, 0, axis, NT)
+    assert np.array_equal(e8, e8_o)
+    assert np.array_equal(q, q_o)
+    assert cl == c_o
+    if rule == 1:
+        assert c_o == 0                  # rounding the scale up never clips
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_mx_ex_edge_values(dtype):
+    """Every rule and direction, both formats, headroom 0..2, on a tensor with
+    zero / NaN / Inf / subnormal / huge blocks and a ragged column tile."""
+    rng = np.random.default_rng(43)
+    rows, cols = 96, 320          # 320 = 256 + 64: a ragged column tile
+    v = rng.standard_normal((rows, cols)) * np.exp(rng.uniform(-40, 40, size=(rows, 1)))
+    v[:, 5] *= np.exp(rng.uniform(-30, 30))
+    v[0:32, 0] = 0.0
+    v[0, :32] = 0.0
+    v[1, 7] = np.nan
+    v[40, 40] = -np.inf
+    v[3, :] *= 1e-38
+    v[4, 64:] = 3e38
+    x = torch.from_numpy(v.astype(np.float32)).to(dtype).cuda()
+    xb = host_bits(x).reshape(rows, cols)
+    for fmt in (0, 1):
+        for rule in (0, 1, 2):
+            for axis in (0, 1):
+                for h in (0, 2):
+                    q, e8, cl = _mx_ex_gpu(x, fmt, rule, h, axis)
+                    q_o, e8_o, c_o = coracle.mx_cast_ex(xb, fmt, rule, h, axis)
+                    assert np.array_equal(e8, e8_o), (fmt, rule, axis, h)
+                    assert np.array_equal(q, q_o), (fmt, rule, axis, h)
+                    assert cl == c_o, (fmt, rule, axis, h)
+
+
+def test_mx_ex_argument_checks():
+    x = torch.zeros(48, 64, dtype=torch.bfloat16, device="cuda")
+    q = torch.empty(48, 64, dtype=torch.uint8, device="cuda")
+    e8 = torch.empty(2, 64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(F.Fp8qError):
+        F.mx_cast_ex(x, 0, 0, 0, 1, q, e8)          # rows not a multiple of 32
+    with pytest.raises(F.Fp8qError):
+        F.mx_cast_ex(x[:32], 0, 3, 0, 0, q, e8)     # unknown rule
+
+
 # ---------------------------------------------------------------------------
 # edge cases of the per-tensor path
 # ---------------------------------------------------------------------------
@@ -361,6 +423,66 @@ def test_resume_equals_continuous():
     c = F.ScaledCast(0, window=4, margin=1)
     c.set_history(saved, prev_e)
     part += [c(x)[0].cpu() for x in xs[8:]]
+    assert all(torch.equal(u, v) for u, v in zip(full, part))
+    for g in (a, b, c):
+        g.close()
+
+
+@pytest.mark.parametrize("estimator,alpha,interval,window", [
+    (1, 0.5, 1, 0), (1, 0.1, 1, 4), (1, 1.0, 1, 0), (0, 1.0, 3, 1), (0, 1.0, 4, 16), (1, 0.25, 2, 2)])
+def test_estimators_on_spike_sequence(estimator, alpha, interval, window):
+    """Exponential smoothing and the recompute interval on the spike
+    sequence (bf16 [2048, 2048], x8 spike at step 9), every step compared."""
+    g = F.ScaledCast(F.E4M3, window, 0, 0, estimator=estimator, alpha=alpha, interval=interval)
+    o = policy.ScalingState(0, window, 0, 0, estimator=estimator, alpha=alpha, interval=interval)
+    xs = [synthetic.spike_step(s, "cuda", shape=(2048, 2048)) for s in range(16)]
+    run_steps(g, o, xs)
+    avg, steps = F.fp8q_get_estimator_state(g.handle)
+    assert steps == 16
+    if estimator == 1:
+        assert np.float32(avg) == o.avg
+    g.close()
+
+
+def test_estimators_mixed_in_one_group():
+    """One grouped launch holding max-window, smoothed and interval handles."""
+    rng = np.random.default_rng(19)
+    cfg = [(0, 16, 0, 1.0, 1), (1, 0, 1, 0.3, 1), (0, 1, 0, 1.0, 3), (1, 4, 1, 0.5, 2)] * 5
+    hs = [F.fp8q_create_ex(f, w, 0, 0, est, a, k) for f, w, est, a, k in cfg]
+    orc = [policy.ScalingState(f, w, 0, 0, estimator=est, alpha=a, interval=k) for f, w, est, a, k in cfg]
+    for t in range(6):
+        xs = [_special_tensor(int(n), torch.bfloat16, 100 * t + i) * float(np.exp(rng.uniform(-3, 3)))
+              for i, n in enumerate(rng.choice([100, 8192, 20000, 70000], len(cfg)))]
+        qs = [torch.empty(x.numel(), dtype=torch.uint8, device="cuda") for x in xs]
+        sinv = torch.empty(len(cfg), dtype=torch.float32, device="cuda")
+        amax = torch.empty(len(cfg), dtype=torch.float32, device="cuda")
+        clipped = torch.empty(len(cfg), dtype=torch.int64, device="cuda")
+        F.fp8q_cast_multi(hs, xs, qs, sinv, amax, clipped)
+        torch.cuda.synchronize()
+        sb, ab, cb = f32bits(sinv), f32bits(amax), clipped.cpu().numpy()
+        for i, x in enumerate(xs):
+            q_o, a_o, s_o, c_o, _ = orc[i].step(host_bits(x), NT)
+            assert np.array_equal(qs[i].cpu().numpy(), q_o.reshape(-1)), (t, i)
+            assert (ab[i], sb[i], int(cb[i])) == (a_o, s_o, c_o), (t, i)
+    for h in hs:
+        F.fp8q_destroy(h)
+
+
+def test_estimator_resume_equals_continuous():
+    """Smoothed estimator with interval 3: 12 casts straight == 5 casts,
+    save (history, exponent, average, steps), restore, 7 casts."""
+    xs = [synthetic.spike_step(s, "cuda", shape=(256, 1024)) for s in range(12)]
+    kw = dict(estimator=1, alpha=0.3, interval=3)
+    a = F.ScaledCast(0, 4, 0, 0, **kw)
+    full = [a(x)[0].cpu() for x in xs]
+    b = F.ScaledCast(0, 4, 0, 0, **kw)
+    part = [b(x)[0].cpu() for x in xs[:5]]
+    hist, (prev_e, _) = b.history(), b.state()
+    avg, steps = F.fp8q_get_estimator_state(b.handle)
+    c = F.ScaledCast(0, 4, 0, 0, **kw)
+    c.set_history(hist, prev_e)
+    F.fp8q_set_estimator_state(c.handle, avg, steps)
+    part += [c(x)[0].cpu() for x in xs[5:]]
     assert all(torch.equal(u, v) for u, v in zip(full, part))
     for g in (a, b, c):
         g.close()

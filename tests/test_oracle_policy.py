@@ -160,3 +160,59 @@ def test_spike_overflows_one_window_late(orc):
     clips_recent = [recent.step(x.view(np.uint32))[3] for x in seq]
     clips_window = [window.step(x.view(np.uint32))[3] for x in seq]
     assert clips_recent[-1] > 0 and clips_window[-1] == 0
+
+
+def _estimator_traces():
+    rows = []
+    with open(os.path.join(GOLDEN, "estimator_traces.txt")) as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            head, am, es, cl = [p.strip() for p in line.split("|")]
+            name, w, est, alpha, interval = head.split()
+            rows.append((name, int(w), {"max": policy.MAX_WINDOW, "ema": policy.EMA}[est],
+                         float(alpha), int(interval), [_parse_amax(a) for a in am.split()],
+                         [int(e) for e in es.split()], [int(c) for c in cl.split()]))
+    return rows
+
+
+@pytest.mark.parametrize("row", _estimator_traces(), ids=lambda r: r[0])
+def test_estimator_traces(row):
+    name, w, est, alpha, interval, amaxes, es, clipped = row
+    st = policy.ScalingState(0, w, 0, 0, estimator=est, alpha=alpha, interval=interval)
+    for t, a in enumerate(amaxes):
+        _, _, _, n_clip, e = st.step(_step_tensor(a))
+        assert (e, n_clip) == (es[t], clipped[t]), (name, t)
+
+
+def test_smoothing_with_alpha_one_is_most_recent():
+    """A running average with coefficient 1 is the previous step's amax."""
+    rng = np.random.default_rng(14)
+    a = policy.ScalingState(0, window=0, estimator=policy.EMA, alpha=1.0)
+    b = policy.ScalingState(0, window=1)
+    for t in range(30):
+        x = (rng.standard_normal(500) * np.exp(rng.uniform(-4, 4))).astype(np.float32).view(np.uint32)
+        assert a.step(x)[4] == b.step(x)[4]
+
+
+def test_interval_one_is_the_plain_policy():
+    rng = np.random.default_rng(15)
+    a = policy.ScalingState(1, window=4, margin=1, interval=1)
+    b = policy.ScalingState(1, window=4, margin=1)
+    for t in range(30):
+        x = (rng.standard_normal(500) * np.exp(rng.uniform(-4, 4))).astype(np.float32).view(np.uint32)
+        ra, rb = a.step(x), b.step(x)
+        assert ra[3:] == rb[3:] and np.array_equal(ra[0], rb[0])
+
+
+def test_smoothing_update_is_fp32_without_fma():
+    """The running average is three fp32 roundings: sub, mul, add."""
+    st = policy.ScalingState(0, window=0, estimator=policy.EMA, alpha=0.1)
+    vals = [1.0, 3.3, 1e-3, 7.77]
+    for v in vals:
+        st.step(np.array([v], dtype=np.float32).view(np.uint32))
+    avg = np.float32(1.0)
+    for v in vals[1:]:
+        d = np.float32(np.float32(v) - avg)
+        avg = np.float32(avg + np.float32(np.float32(0.1) * d))
+    assert st.avg == avg and st.avg.dtype == np.float32
