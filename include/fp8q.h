@@ -167,6 +167,40 @@ FP8Q_API int fp8q_cast_multi(const fp8q_handle* hs, const void* const* xs, const
                              float* d_amax, unsigned long long* d_clipped, int count,
                              void* stream);
 
+/* fp8q_cast_multi with two more per-tensor counts (DEVICE arrays of length
+ * count, or NULL):
+ *   d_nonfinite  NaN or +-Inf inputs ("Mixed Precision FP16/BF16/FP8": the
+ *                Inf/NaN detection that dynamic loss scaling reacts to)
+ *   d_underflow  finite nonzero inputs whose 8-bit result is a zero ("what
+ *                actually breaks low precision training": underflow rates)
+ * Counting underflow adds work to every element; with d_underflow NULL the
+ * launch is the same as fp8q_cast_multi's.  Non-finite inputs are counted on
+ * the path that already handles them, at no cost otherwise. */
+FP8Q_API int fp8q_cast_multi_ex(const fp8q_handle* hs, const void* const* xs, const int* dtypes,
+                                const int64_t* ns, uint8_t* const* qs, float* d_scale_inv,
+                                float* d_amax, unsigned long long* d_clipped,
+                                unsigned long long* d_nonfinite, unsigned long long* d_underflow,
+                                int count, void* stream);
+
+/* Dynamic loss scaling, device-resident ("Mixed Precision FP16/BF16/FP8"
+ * mind-map card: multiply the loss by S, commonly 2^24 or 1024; on Inf/NaN
+ * set S <- S/2 and skip the step; after a period without overflow double S).
+ * The period is growth_interval clean steps in a row; S stays within
+ * [min_scale, max_scale].  Allocates its state with cudaMalloc. */
+typedef struct fp8q_loss_scaler_state* fp8q_loss_scaler;
+FP8Q_API int fp8q_loss_scaler_create(float init_scale, int growth_interval, float min_scale,
+                                     float max_scale, fp8q_loss_scaler* out);
+FP8Q_API int fp8q_loss_scaler_destroy(fp8q_loss_scaler ls);
+/* One step: d_nonfinite is a DEVICE array of `count` non-finite counts (as
+ * written by fp8q_cast_multi_ex for the step's gradient casts); the step is
+ * non-finite when any is nonzero.  Writes the new scale to *d_scale and 1
+ * (skip the step) or 0 to *d_skip (device pointers, either may be NULL).
+ * One single-CTA launch. */
+FP8Q_API int fp8q_loss_scaler_update(fp8q_loss_scaler ls, const unsigned long long* d_nonfinite,
+                                     int count, float* d_scale, int* d_skip, void* stream);
+/* Current scale and clean-step streak; blocks until the last update ran. */
+FP8Q_API int fp8q_loss_scaler_read(fp8q_loss_scaler ls, float* scale, int* good_steps);
+
 /* MX block-scaled cast ("what actually breaks low precision training", "What
  * the measurements said"): x is a row-major [rows, cols] tensor; each 32
  * consecutive elements of a row share E = floor(log2(block amax)) -

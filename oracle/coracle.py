@@ -63,6 +63,8 @@ def lib():
         L.orc_mx_exp_rule.restype = c_int
         L.orc_mx_cast_ex.argtypes = [c_p, c_int, c_i64, c_i64, c_int, c_int, c_int, c_int, c_p, c_p, c_int]
         L.orc_mx_cast_ex.restype = c_i64
+        L.orc_count_special.argtypes = [c_p, c_int, c_i64, c_p, ctypes.POINTER(c_i64), ctypes.POINTER(c_i64)]
+        L.orc_count_special.restype = None
         L.orc_stats.argtypes = [c_p, c_int, c_i64, c_p, c_int, c_int, c_p, c_int]
         L.orc_stats.restype = None
         L.orc_mx_stats.argtypes = [c_p, c_int, c_i64, c_i64, c_p, c_p, c_int, c_p, c_int]
@@ -180,4 +182,13 @@ def mx_cast_ex(x: np.ndarray, fmt: int, rule: int, headroom: int, axis: int, nth
     clipped = lib().orc_mx_cast_ex(_ptr(x), _dtype_of(x), rows, cols, fmt, rule, headroom, axis,
                                    _ptr(q), _ptr(e8), nthreads)
     return q, e8, int(clipped)
+
+
+def count_special(x: np.ndarray, q: np.ndarray):
+    """(non-finite inputs, underflowed elements) of a cast x -> q."""
+    x = np.ascontiguousarray(x).reshape(-1)
+    q = np.ascontiguousarray(q).reshape(-1)
+    nf, uf = ctypes.c_int64(), ctypes.c_int64()
+    lib().orc_count_special(_ptr(x), _dtype_of(x), x.size, _ptr(q), ctypes.byref(nf), ctypes.byref(uf))
+    return int(nf.value), int(uf.value)
 

@@ -467,3 +467,23 @@ int64_t orc_mx_cast_ex(const void* x, int dtype, int64_t rows, int64_t cols, int
     return clipped;
 }
 
+/* --------------------------------------------------------------------------
+ * Counts that drive dynamic loss scaling ("Mixed Precision FP16/BF16/FP8":
+ * on Inf/NaN halve the loss scale and skip the step) and the underflow rate
+ * ("what actually breaks low precision training", "What the measurements
+ * said": clip rates and underflow rates).  Readings: an element is
+ * non-finite when the input is NaN or +-Inf; it underflowed when the input is
+ * finite and nonzero and its 8-bit result is a zero (+0 or -0).
+ * ------------------------------------------------------------------------ */
+void orc_count_special(const void* x, int dtype, int64_t n, const uint8_t* q,
+                       int64_t* nonfinite, int64_t* underflow) {
+    int64_t nf = 0, uf = 0;
+    for (int64_t i = 0; i < n; i++) {
+        uint32_t a = load_bits(x, dtype, i) & 0x7FFFFFFFu;
+        if (a >= 0x7F800000u) nf++;
+        else if (a != 0 && (q[i] & 0x7Fu) == 0) uf++;
+    }
+    *nonfinite = nf;
+    *underflow = uf;
+}
+

@@ -112,3 +112,32 @@ class ScalingState:
             del self.hist[:-self.window]
         self.prev_e = e
         self.steps += 1
+
+
+class LossScaler:
+    """Dynamic loss scaling ("Mixed Precision FP16/BF16/FP8" mind-map card:
+    multiply the loss by S; on Inf/NaN set S <- S/2 and skip the step; after
+    a period without overflow double S).  Readings: the period is
+    `growth_interval` consecutive clean steps; S stays within
+    [min_scale, max_scale]; a step is non-finite when any of its casts saw a
+    NaN or Inf input."""
+
+    def __init__(self, init_scale: float, growth_interval: int,
+                 min_scale: float = 1.0, max_scale: float = 2.0 ** 24):
+        self.scale = np.float32(init_scale)
+        self.growth_interval = growth_interval
+        self.min_scale, self.max_scale = np.float32(min_scale), np.float32(max_scale)
+        self.good = 0
+
+    def update(self, nonfinite_counts) -> bool:
+        """Returns True when the step must be skipped."""
+        if any(int(c) > 0 for c in nonfinite_counts):
+            self.scale = max(self.min_scale, np.float32(self.scale * np.float32(0.5)))
+            self.good = 0
+            return True
+        self.good += 1
+        if self.good >= self.growth_interval:
+            self.scale = min(self.max_scale, np.float32(self.scale * np.float32(2.0)))
+            self.good = 0
+        return False
+

@@ -187,8 +187,9 @@ FP8Q_API int fp8q_destroy(fp8q_handle h) {
 // the tensors that need it, then the fused cast.
 static int plan_and_launch(const fp8q_handle* hs, const void* const* xs, const int* dtypes,
                            const int64_t* ns, uint8_t* const* qs, float* d_scale_inv,
-                           float* d_amax, unsigned long long* d_clipped, int count,
-                           cudaStream_t s) {
+                           float* d_amax, unsigned long long* d_clipped,
+                           unsigned long long* d_nonfinite, unsigned long long* d_underflow,
+                           int count, cudaStream_t s) {
   for (int base = 0; base < count; base += kMaxGroup) {
     const int m = std::min(kMaxGroup, count - base);
     std::vector<TensorDesc> all(m), pre;
@@ -233,6 +234,8 @@ static int plan_and_launch(const fp8q_handle* hs, const void* const* xs, const i
     gh.scale_inv = d_scale_inv;
     gh.amax = d_amax;
     gh.clipped = d_clipped;
+    gh.nonfinite = d_nonfinite;
+    gh.underflow = d_underflow;
     gh.total_chunks = (int32_t)chunks;
     gh.out_offset = base;
     cudaError_t e = launch_cast_group(gh, all.data(), m, s, &launches);
@@ -265,14 +268,15 @@ FP8Q_API int fp8q_cast(fp8q_handle h, const void* x, int dtype, int64_t n, uint8
   if (st != FP8Q_OK) return st;
   st = check_device(h);
   if (st != FP8Q_OK) return st;
-  return plan_and_launch(&h, &x, &dtype, &n, &q, d_scale_inv, d_amax, d_clipped, 1,
-                         reinterpret_cast<cudaStream_t>(stream));
+  return plan_and_launch(&h, &x, &dtype, &n, &q, d_scale_inv, d_amax, d_clipped, nullptr, nullptr,
+                         1, reinterpret_cast<cudaStream_t>(stream));
 }
 
-FP8Q_API int fp8q_cast_multi(const fp8q_handle* hs, const void* const* xs, const int* dtypes,
-                             const int64_t* ns, uint8_t* const* qs, float* d_scale_inv,
-                             float* d_amax, unsigned long long* d_clipped, int count,
-                             void* stream) {
+FP8Q_API int fp8q_cast_multi_ex(const fp8q_handle* hs, const void* const* xs, const int* dtypes,
+                                const int64_t* ns, uint8_t* const* qs, float* d_scale_inv,
+                                float* d_amax, unsigned long long* d_clipped,
+                                unsigned long long* d_nonfinite, unsigned long long* d_underflow,
+                                int count, void* stream) {
   if (count <= 0 || !hs || !xs || !dtypes || !ns || !qs) return FP8Q_EINVAL;
   for (int i = 0; i < count; ++i) {
     int st = check_tensor(hs[i], xs[i], dtypes[i], ns[i], qs[i]);
@@ -283,8 +287,102 @@ FP8Q_API int fp8q_cast_multi(const fp8q_handle* hs, const void* const* xs, const
   std::vector<fp8q_handle> sorted(hs, hs + count);
   std::sort(sorted.begin(), sorted.end());
   if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end()) return FP8Q_EINVAL;
-  return plan_and_launch(hs, xs, dtypes, ns, qs, d_scale_inv, d_amax, d_clipped, count,
-                         reinterpret_cast<cudaStream_t>(stream));
+  return plan_and_launch(hs, xs, dtypes, ns, qs, d_scale_inv, d_amax, d_clipped, d_nonfinite,
+                         d_underflow, count, reinterpret_cast<cudaStream_t>(stream));
+}
+
+FP8Q_API int fp8q_cast_multi(const fp8q_handle* hs, const void* const* xs, const int* dtypes,
+                             const int64_t* ns, uint8_t* const* qs, float* d_scale_inv,
+                             float* d_amax, unsigned long long* d_clipped, int count,
+                             void* stream) {
+  return fp8q_cast_multi_ex(hs, xs, dtypes, ns, qs, d_scale_inv, d_amax, d_clipped, nullptr, nullptr,
+                            count, stream);
+}
+
+static const uint32_t kScalerMagic = 0x1055CA1Eu;
+
+}  // extern "C"
+
+struct fp8q_loss_scaler_state {
+  uint32_t magic;
+  int device;
+  LossScaleState* dev;
+  cudaEvent_t last;
+  bool has_last;
+};
+
+extern "C" {
+
+FP8Q_API int fp8q_loss_scaler_create(float init_scale, int growth_interval, float min_scale,
+                                     float max_scale, fp8q_loss_scaler* out) {
+  if (!out) return FP8Q_EINVAL;
+  *out = nullptr;
+  if (!(min_scale > 0.0f) || !(max_scale >= min_scale) || !(init_scale >= min_scale) ||
+      !(init_scale <= max_scale) || growth_interval < 1)
+    return FP8Q_EINVAL;
+  fp8q_loss_scaler_state* ls = new (std::nothrow) fp8q_loss_scaler_state();
+  if (!ls) return FP8Q_ENOMEM;
+  cudaError_t e = cudaGetDevice(&ls->device);
+  if (e != cudaSuccess) { delete ls; return fail_cuda(e); }
+  e = cudaMalloc(reinterpret_cast<void**>(&ls->dev), sizeof(LossScaleState));
+  if (e != cudaSuccess) { delete ls; return e == cudaErrorMemoryAllocation ? FP8Q_ENOMEM : fail_cuda(e); }
+  LossScaleState init;
+  std::memset(&init, 0, sizeof init);
+  init.scale = init_scale;
+  init.min_scale = min_scale;
+  init.max_scale = max_scale;
+  init.growth_interval = growth_interval;
+  e = cudaMemcpy(ls->dev, &init, sizeof init, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ls->last, cudaEventDisableTiming);
+  if (e != cudaSuccess) { cudaFree(ls->dev); delete ls; return fail_cuda(e); }
+  ls->has_last = false;
+  ls->magic = kScalerMagic;
+  *out = ls;
+  return FP8Q_OK;
+}
+
+FP8Q_API int fp8q_loss_scaler_destroy(fp8q_loss_scaler ls) {
+  if (!ls) return FP8Q_OK;
+  if (ls->magic != kScalerMagic) return FP8Q_EHANDLE;
+  if (ls->has_last) cudaEventSynchronize(ls->last);
+  cudaEventDestroy(ls->last);
+  cudaError_t e = cudaFree(ls->dev);
+  ls->magic = 0;
+  delete ls;
+  return e == cudaSuccess ? FP8Q_OK : fail_cuda(e);
+}
+
+FP8Q_API int fp8q_loss_scaler_update(fp8q_loss_scaler ls, const unsigned long long* d_nonfinite,
+                                     int count, float* d_scale, int* d_skip, void* stream) {
+  if (!ls || ls->magic != kScalerMagic) return FP8Q_EHANDLE;
+  if (count < 0 || (count > 0 && !d_nonfinite)) return FP8Q_EINVAL;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev != ls->device) return FP8Q_EDEVICE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int launches = 0;
+  e = launch_loss_scale_update(ls->dev, d_nonfinite, count, d_scale, d_skip, s, &launches);
+  g_launches += launches;
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = cudaEventRecord(ls->last, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  ls->has_last = true;
+  return FP8Q_OK;
+}
+
+FP8Q_API int fp8q_loss_scaler_read(fp8q_loss_scaler ls, float* scale, int* good_steps) {
+  if (!ls || ls->magic != kScalerMagic) return FP8Q_EHANDLE;
+  if (ls->has_last) {
+    cudaError_t e = cudaEventSynchronize(ls->last);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  LossScaleState d;
+  cudaError_t e = cudaMemcpy(&d, ls->dev, sizeof d, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (scale) *scale = d.scale;
+  if (good_steps) *good_steps = d.good;
+  return FP8Q_OK;
 }
 
 FP8Q_API int mx_cast_ex(const void* x, int dtype, int64_t rows, int64_t cols, int format,

@@ -78,16 +78,18 @@ __device__ __forceinline__ uint32_t chunk_absmax(const uint4 (&r)[kUnroll]) {
 // Cast a loaded chunk with scale s and store it.  m = the thread's abs-max
 // over its slots (fp32 bits); the exact per-element pass runs only when m
 // exceeds the no-clip bound (rare: clipping, Inf or NaN present).
-template <int DT, int FMT, bool FULL>
+template <int DT, int FMT, bool FULL, bool UF>
 __device__ __forceinline__ void cast_store_chunk(const uint4 (&r)[kUnroll], uint8_t* q, int64_t rem,
                                                  float s, uint32_t m, uint32_t bound,
-                                                 uint32_t& clip) {
+                                                 uint32_t ubound, uint32_t& clip,
+                                                 uint32_t* s_nonfinite, uint32_t& under) {
   constexpr int EPL = Tr<DT>::EPL;
   const bool slow = m > bound;
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u) {
     uint2 o = cast_load<DT, FMT>(r[u], s);
-    if (slow) fix_load<DT, FMT>(r[u], s, o, clip);
+    if (slow) fix_load<DT, FMT>(r[u], s, o, clip, s_nonfinite);
+    if (UF) under += underflow_load<DT>(r[u], ubound);   // zero-filled tail slots count 0
     if (FULL) {
       if (DT == FP8Q_BF16) __stcs(reinterpret_cast<uint2*>(q) + threadIdx.x + u * kThreads, o);
       else __stcs(reinterpret_cast<unsigned int*>(q) + threadIdx.x + u * kThreads, o.x);
@@ -156,11 +158,15 @@ __device__ void finish_tensor(DevState* st, const GroupHeader& h, int t, int e) 
   __threadfence();
   uint32_t a = atomicAdd(&st->amax_acc, 0u);
   const unsigned long long cl = atomicAdd(&st->clip_acc, 0ull);
+  const unsigned long long nf = atomicAdd(&st->nonfinite_acc, 0ull);
+  const unsigned long long uf = atomicAdd(&st->underflow_acc, 0ull);
   if (a > 0x7F800000u) a = 0x7FC00000u;        // canonical NaN
   const int idx = h.out_offset + t;
   if (h.amax) h.amax[idx] = __uint_as_float(a);
   if (h.scale_inv) h.scale_inv[idx] = pow2f(-e);
   if (h.clipped) h.clipped[idx] = cl;
+  if (h.nonfinite) h.nonfinite[idx] = nf;
+  if (h.underflow) h.underflow[idx] = uf;
   const int W = st->window;
   if (W > 0) {
     const int hd = st->head;
@@ -180,15 +186,17 @@ __device__ void finish_tensor(DevState* st, const GroupHeader& h, int t, int e) 
   st->phase = (st->phase + 1 >= st->interval) ? 0 : st->phase + 1;
   st->amax_acc = 0u;
   st->clip_acc = 0ull;
+  st->nonfinite_acc = 0ull;
+  st->underflow_acc = 0ull;
   st->pre_amax = 0u;
   st->ticket = 0u;
 }
 
 // Chunks [c0, c1) of tensor d (tensor-local chunk indices).
-template <int DT, int FMT>
+template <int DT, int FMT, bool UF>
 __device__ void cast_segment(const TensorDesc& d, int c0, int c1, int mode, int* s_e,
                              uint32_t* red_m, uint32_t* red_c, uint32_t& lmax, uint32_t& lclip,
-                             int& e_out) {
+                             uint32_t* s_nonfin, uint32_t& lunder, int& e_out) {
   constexpr int CH = Tr<DT>::CHUNK, ESZ = Tr<DT>::ESZ;
   const char* x = reinterpret_cast<const char*>(d.x);
   if (mode == kCurrentLocal) {
@@ -202,7 +210,8 @@ __device__ void cast_segment(const TensorDesc& d, int c0, int c1, int mode, int*
     if (threadIdx.x == 0) *s_e = state_exp(d.st, bm > 0x7F800000u ? 0x7FC00000u : bm);
     __syncthreads();
     const int e = *s_e;
-    cast_store_chunk<DT, FMT, false>(r, d.q, d.n, pow2f(e), m, no_clip_bound(FMT, e), lclip);
+    cast_store_chunk<DT, FMT, false, UF>(r, d.q, d.n, pow2f(e), m, no_clip_bound(FMT, e),
+                                         UF ? underflow_bound(FMT, e) : 0u, lclip, s_nonfin, lunder);
     lmax = max(lmax, m);
     e_out = e;
     return;
@@ -212,6 +221,7 @@ __device__ void cast_segment(const TensorDesc& d, int c0, int c1, int mode, int*
   const int e = *s_e;
   const float s = pow2f(e);
   const uint32_t bound = no_clip_bound(FMT, e);
+  const uint32_t ubound = UF ? underflow_bound(FMT, e) : 0u;
   for (int c = c0; c < c1; ++c) {
     const int64_t base = (int64_t)c * CH;
     const int64_t rem = d.n - base;
@@ -220,12 +230,12 @@ __device__ void cast_segment(const TensorDesc& d, int c0, int c1, int mode, int*
       load_chunk<DT, true>(x + base * ESZ, rem, r);
       const uint32_t m = chunk_absmax<DT>(r);
       lmax = max(lmax, m);
-      cast_store_chunk<DT, FMT, true>(r, d.q + base, rem, s, m, bound, lclip);
+      cast_store_chunk<DT, FMT, true, UF>(r, d.q + base, rem, s, m, bound, ubound, lclip, s_nonfin, lunder);
     } else {
       load_chunk<DT, false>(x + base * ESZ, rem, r);
       const uint32_t m = chunk_absmax<DT>(r);
       lmax = max(lmax, m);
-      cast_store_chunk<DT, FMT, false>(r, d.q + base, rem, s, m, bound, lclip);
+      cast_store_chunk<DT, FMT, false, UF>(r, d.q + base, rem, s, m, bound, ubound, lclip, s_nonfin, lunder);
     }
   }
   e_out = e;
@@ -256,10 +266,12 @@ __device__ __forceinline__ int first_tensor(const GroupParams<MAXT>& p, int c) {
   return lo;
 }
 
-template <int MAXT>
-__global__ void __launch_bounds__(kThreads, 4) cast_group_kernel(const __grid_constant__ GroupParams<MAXT> p) {
+template <int MAXT, bool UF>
+__global__ void __launch_bounds__(kThreads, UF ? 3 : 4) cast_group_kernel(const __grid_constant__ GroupParams<MAXT> p) {
   __shared__ int s_e;
-  __shared__ uint32_t red_m[kThreads / 32], red_c[kThreads / 32];
+  __shared__ uint32_t s_nonfin;                   // non-finite inputs of the current segment
+  __shared__ uint32_t red_m[kThreads / 32], red_c[kThreads / 32], red_u[kThreads / 32];
+  if (threadIdx.x == 0) s_nonfin = 0u;            // published by the first __syncthreads below
   const int total = p.h.total_chunks;
   int c = (int)(((long long)blockIdx.x * total) / gridDim.x);
   const int c_end = (int)(((long long)(blockIdx.x + 1) * total) / gridDim.x);
@@ -271,20 +283,32 @@ __global__ void __launch_bounds__(kThreads, 4) cast_group_kernel(const __grid_co
     const int t_end = (t + 1 < p.h.count) ? p.d[t + 1].chunk_begin : total;
     const int seg_end = min(c_end, t_end);
     const int mode = (d.flags >> 2) & 3;
-    uint32_t lmax = 0, lclip = 0;
+    uint32_t lmax = 0, lclip = 0, lunder = 0;
     int e = 0;
+    const int c0 = c - t_begin, c1 = seg_end - t_begin;
     switch (d.flags & 3) {
-      case 0: cast_segment<FP8Q_F32, FP8Q_E4M3>(d, c - t_begin, seg_end - t_begin, mode, &s_e, red_m, red_c, lmax, lclip, e); break;
-      case 1: cast_segment<FP8Q_BF16, FP8Q_E4M3>(d, c - t_begin, seg_end - t_begin, mode, &s_e, red_m, red_c, lmax, lclip, e); break;
-      case 2: cast_segment<FP8Q_F32, FP8Q_E5M2>(d, c - t_begin, seg_end - t_begin, mode, &s_e, red_m, red_c, lmax, lclip, e); break;
-      default: cast_segment<FP8Q_BF16, FP8Q_E5M2>(d, c - t_begin, seg_end - t_begin, mode, &s_e, red_m, red_c, lmax, lclip, e); break;
+      case 0: cast_segment<FP8Q_F32, FP8Q_E4M3, UF>(d, c0, c1, mode, &s_e, red_m, red_c, lmax, lclip, &s_nonfin, lunder, e); break;
+      case 1: cast_segment<FP8Q_BF16, FP8Q_E4M3, UF>(d, c0, c1, mode, &s_e, red_m, red_c, lmax, lclip, &s_nonfin, lunder, e); break;
+      case 2: cast_segment<FP8Q_F32, FP8Q_E5M2, UF>(d, c0, c1, mode, &s_e, red_m, red_c, lmax, lclip, &s_nonfin, lunder, e); break;
+      default: cast_segment<FP8Q_BF16, FP8Q_E5M2, UF>(d, c0, c1, mode, &s_e, red_m, red_c, lmax, lclip, &s_nonfin, lunder, e); break;
     }
     __syncthreads();                       // red_* reuse after the local-mode reduction
     block_reduce(lmax, lclip, red_m, red_c);
+    if (UF) {
+      lunder = __reduce_add_sync(0xFFFFFFFFu, lunder);
+      if ((threadIdx.x & 31) == 0) red_u[threadIdx.x >> 5] = lunder;
+      __syncthreads();
+      if (threadIdx.x == 0)
+        for (int i = 1; i < kThreads / 32; ++i) lunder += red_u[i];
+    }
     if (threadIdx.x == 0) {
       DevState* st = d.st;
+      const uint32_t lnonfin = s_nonfin;   // all slow-path adds happened before the reduction's barrier
+      s_nonfin = 0u;
       if (lmax) atomicMax(&st->amax_acc, lmax);
       if (lclip) atomicAdd(&st->clip_acc, (unsigned long long)lclip);
+      if (lnonfin) atomicAdd(&st->nonfinite_acc, (unsigned long long)lnonfin);
+      if (UF && lunder) atomicAdd(&st->underflow_acc, (unsigned long long)lunder);
       __threadfence();
       const unsigned done = (unsigned)(seg_end - c);
       const unsigned prev = atomicAdd(&st->ticket, done);
@@ -330,14 +354,15 @@ static int resident_ctas(K kernel) {
   return nb;
 }
 
-template <int MAXT, bool CAST>
+template <int MAXT, int KIND>   // KIND 0: amax pre-pass, 1: cast, 2: cast + underflow count
 static cudaError_t launch_group_t(const GroupHeader& h, const TensorDesc* d, int count,
                                   cudaStream_t s, int* launches) {
   GroupParams<MAXT> p;
   p.h = h;
   p.h.count = count;
   for (int i = 0; i < count; ++i) p.d[i] = d[i];
-  auto kern = CAST ? cast_group_kernel<MAXT> : amax_group_kernel<MAXT>;
+  auto kern = KIND == 0 ? amax_group_kernel<MAXT>
+                        : (KIND == 1 ? cast_group_kernel<MAXT, false> : cast_group_kernel<MAXT, true>);
   static int occ = 0;
   if (occ == 0) occ = resident_ctas(kern);
   const int dev = device_of_current();
@@ -349,22 +374,54 @@ static cudaError_t launch_group_t(const GroupHeader& h, const TensorDesc* d, int
   return cudaGetLastError();
 }
 
-template <bool CAST>
+template <int KIND>
 static cudaError_t launch_group(const GroupHeader& h, const TensorDesc* d, int count,
                                 cudaStream_t s, int* launches) {
-  if (count <= 1) return launch_group_t<1, CAST>(h, d, count, s, launches);
-  if (count <= 32) return launch_group_t<32, CAST>(h, d, count, s, launches);
-  return launch_group_t<kMaxGroup, CAST>(h, d, count, s, launches);
+  if (count <= 1) return launch_group_t<1, KIND>(h, d, count, s, launches);
+  if (count <= 32) return launch_group_t<32, KIND>(h, d, count, s, launches);
+  return launch_group_t<kMaxGroup, KIND>(h, d, count, s, launches);
 }
 
 cudaError_t launch_cast_group(const GroupHeader& h, const TensorDesc* d, int count,
                               cudaStream_t s, int* launches) {
-  return launch_group<true>(h, d, count, s, launches);
+  return h.underflow ? launch_group<2>(h, d, count, s, launches) : launch_group<1>(h, d, count, s, launches);
 }
 
 cudaError_t launch_amax_group(const GroupHeader& h, const TensorDesc* d, int count,
                               cudaStream_t s, int* launches) {
-  return launch_group<false>(h, d, count, s, launches);
+  return launch_group<0>(h, d, count, s, launches);
+}
+
+// ---- dynamic loss scaling ----------------------------------------------------
+//
+// One CTA: "was any input of this step NaN or Inf?" over the per-tensor
+// non-finite counts, then the state machine ("Mixed Precision FP16/BF16/FP8":
+// on Inf/NaN halve the scale and skip the step; after growth_interval clean
+// steps in a row double it), clamped to [min_scale, max_scale].
+__global__ void loss_scale_update_kernel(LossScaleState* st, const unsigned long long* nonfinite,
+                                         int count, float* scale_out, int* skip_out) {
+  int found = 0;
+  for (int i = threadIdx.x; i < count; i += blockDim.x) found |= nonfinite[i] != 0ull;
+  found = __syncthreads_or(found);
+  if (threadIdx.x != 0) return;
+  if (found) {
+    st->scale = fmaxf(st->min_scale, st->scale * 0.5f);
+    st->good = 0;
+  } else if (++st->good >= st->growth_interval) {
+    st->scale = fminf(st->max_scale, st->scale * 2.0f);
+    st->good = 0;
+  }
+  st->last_skip = found;
+  st->updates = st->updates + 1;
+  if (scale_out) *scale_out = st->scale;
+  if (skip_out) *skip_out = found;
+}
+
+cudaError_t launch_loss_scale_update(LossScaleState* st, const unsigned long long* nonfinite, int count,
+                                     float* scale_out, int* skip_out, cudaStream_t s, int* launches) {
+  loss_scale_update_kernel<<<1, kThreads, 0, s>>>(st, nonfinite, count, scale_out, skip_out);
+  ++*launches;
+  return cudaGetLastError();
 }
 
 }  // namespace fp8q

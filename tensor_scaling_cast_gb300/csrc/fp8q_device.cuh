@@ -96,13 +96,16 @@ __device__ __forceinline__ uint2 cast_load(const uint4& v, float s) {
 // chunk exceeds fmax * 2^-e or is not finite: counts the clipped elements
 // and writes NaN inputs as sign|0x7F.
 template <int DT, int FMT>
-__device__ __forceinline__ void fix_load(const uint4& v, float s, uint2& o, uint32_t& clip) {
+__device__ __forceinline__ void fix_load(const uint4& v, float s, uint2& o, uint32_t& clip,
+                                         uint32_t* s_nonfinite) {
   constexpr int EPL = DT == FP8Q_BF16 ? 8 : 4;
+  uint32_t nonfinite = 0;
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
     const uint32_t b = elem_bits<DT>(v, j);
     const float f = __uint_as_float(b) * s;
     clip += clips<FMT>(f) ? 1u : 0u;
+    nonfinite += (b & 0x7FFFFFFFu) >= 0x7F800000u ? 1u : 0u;
     if ((b & 0x7FFFFFFFu) > 0x7F800000u) {
       const uint32_t byte = ((b >> 31) << 7) | 0x7Fu;
       const int sh = (j & 3) * 8;
@@ -110,6 +113,40 @@ __device__ __forceinline__ void fix_load(const uint4& v, float s, uint2& o, uint
       else o.y = (o.y & ~(0xFFu << sh)) | (byte << sh);
     }
   }
+  // rare path: a shared-memory counter keeps the common path's registers free
+  if (nonfinite) atomicAdd(s_nonfinite, nonfinite);
+}
+
+// fp32 bits of the largest |x| whose scaled value x * 2^e rounds to zero:
+// half the smallest subnormal (2^-10 for E4M3, 2^-17 for E5M2; the tie goes
+// to the even zero) times 2^-e; 0 when that is below the smallest fp32.
+__device__ __forceinline__ uint32_t underflow_bound(int fmt, int e) {
+  const int k = (fmt == FP8Q_E4M3 ? -10 : -17) - e;
+  if (k >= -126) return (uint32_t)(k + 127) << 23;
+  if (k >= -149) return 1u << (k + 149);
+  return 0u;
+}
+
+// Inputs of one 16-byte load that underflow (0 < |x| <= bound).  bf16: two
+// per word, compared in place: (B|0x8000) - a keeps bit 15 iff a <= B, and
+// a + 0x7FFF sets bit 15 iff a >= 1 (no carry crosses the half-words).
+template <int DT>
+__device__ __forceinline__ uint32_t underflow_load(const uint4& v, uint32_t bound) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t n = 0;
+  if (DT == FP8Q_BF16) {
+    const uint32_t b16 = bound >> 16;
+    const uint32_t bb = (b16 | (b16 << 16)) | 0x80008000u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t a = w[i] & 0x7FFF7FFFu;
+      n += __popc((bb - a) & (a + 0x7FFF7FFFu) & 0x80008000u);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) n += ((w[i] & 0x7FFFFFFFu) - 1u < bound) ? 1u : 0u;
+  }
+  return n;
 }
 
 // Scale exponent from an amax (fp32 bits): the largest e with

@@ -20,6 +20,8 @@ struct __align__(256) DevState {
   uint32_t amax_acc;                // running max of |x| bits, this cast
   uint32_t pre_amax;                // current-scaling pre-pass result
   unsigned long long clip_acc;      // clipped elements, this cast
+  unsigned long long nonfinite_acc; // NaN / Inf inputs, this cast
+  unsigned long long underflow_acc; // finite nonzero inputs cast to zero, this cast
   uint32_t ticket;                  // chunks finished, this cast
   int32_t count;                    // valid ring entries (<= window)
   int32_t head;                     // next ring slot
@@ -52,6 +54,8 @@ struct GroupHeader {
   float* scale_inv;                 // [out_offset + t] outputs, nullable
   float* amax;
   unsigned long long* clipped;
+  unsigned long long* nonfinite;
+  unsigned long long* underflow;    // non-null: the underflow-counting kernel runs
   int32_t count;
   int32_t total_chunks;
   int32_t out_offset;
@@ -83,6 +87,15 @@ cudaError_t launch_stats(const void* x, int dtype, int64_t n, const uint8_t* q, 
                          cudaStream_t s, int* launches);
 
 cudaError_t read_wait_timeouts(unsigned int* count);   // and reset to 0
+
+// Device state of a dynamic loss scaler.
+struct LossScaleState {
+  float scale, min_scale, max_scale;
+  int32_t growth_interval, good, last_skip;
+  long long updates;
+};
+cudaError_t launch_loss_scale_update(LossScaleState* st, const unsigned long long* nonfinite, int count,
+                                     float* scale_out, int* skip_out, cudaStream_t s, int* launches);
 
 int sm_count(int device);
 int record_cuda_error(cudaError_t e);   // keeps the text, returns FP8Q_ECUDA

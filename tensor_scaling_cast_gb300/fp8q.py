@@ -56,6 +56,11 @@ def load() -> ctypes.CDLL:
     L.fp8q_destroy.argtypes = [p]
     L.fp8q_cast.argtypes = [p, p, i, i64, p, p, p, p, p]
     L.fp8q_cast_multi.argtypes = [p, p, p, p, p, p, p, p, i, p]
+    L.fp8q_cast_multi_ex.argtypes = [p, p, p, p, p, p, p, p, p, p, i, p]
+    L.fp8q_loss_scaler_create.argtypes = [f, i, f, f, ctypes.POINTER(p)]
+    L.fp8q_loss_scaler_destroy.argtypes = [p]
+    L.fp8q_loss_scaler_update.argtypes = [p, p, i, p, p, p]
+    L.fp8q_loss_scaler_read.argtypes = [p, ctypes.POINTER(f), ctypes.POINTER(i)]
     L.mx_cast.argtypes = [p, i, i64, i64, i, i, p, p, p, p]
     L.mx_cast_ex.argtypes = [p, i, i64, i64, i, i, i, i, p, p, p, p]
     L.fp8q_amax_history.argtypes = [p, ctypes.POINTER(f), i, ctypes.POINTER(i)]
@@ -71,7 +76,9 @@ def load() -> ctypes.CDLL:
     L.fp8q_strerror.restype = ctypes.c_char_p
     L.fp8q_last_cuda_error.restype = ctypes.c_char_p
     L.fp8q_launch_count.restype = ctypes.c_longlong
-    for name in ("fp8q_create", "fp8q_create_ex", "fp8q_get_estimator_state",
+    for name in ("fp8q_cast_multi_ex", "fp8q_loss_scaler_create", "fp8q_loss_scaler_destroy",
+                 "fp8q_loss_scaler_update", "fp8q_loss_scaler_read",
+                 "fp8q_create", "fp8q_create_ex", "fp8q_get_estimator_state",
                  "fp8q_set_estimator_state", "fp8q_destroy", "fp8q_cast", "fp8q_cast_multi", "mx_cast", "mx_cast_ex",
                  "fp8q_amax_history", "fp8q_scale_state", "fp8q_set_history", "fp8q_reset",
                  "fp8q_error_stats", "mx_error_stats", "fp8q_error_stats_noalloc"):
@@ -172,6 +179,49 @@ def fp8q_cast_multi(hs, xs, qs, scale_inv=None, amax=None, clipped=None, stream=
     N = (ctypes.c_int64 * n)(*[x.numel() for x in xs])
     _check(load().fp8q_cast_multi(H, X, D, N, Q, _ptr(scale_inv), _ptr(amax), _ptr(clipped), n,
                                   _stream(stream)), "fp8q_cast_multi")
+
+
+def fp8q_cast_multi_ex(hs, xs, qs, scale_inv=None, amax=None, clipped=None, nonfinite=None,
+                       underflow=None, stream=None):
+    """fp8q_cast_multi plus int64 CUDA tensors [count] of non-finite and
+    underflow counts (either may be None)."""
+    n = len(hs)
+    H = (ctypes.c_void_p * n)(*hs)
+    X = (ctypes.c_void_p * n)(*[x.data_ptr() for x in xs])
+    Q = (ctypes.c_void_p * n)(*[q.data_ptr() for q in qs])
+    D = (ctypes.c_int * n)(*[_dtype(x) for x in xs])
+    N = (ctypes.c_int64 * n)(*[x.numel() for x in xs])
+    _check(load().fp8q_cast_multi_ex(H, X, D, N, Q, _ptr(scale_inv), _ptr(amax), _ptr(clipped),
+                                     _ptr(nonfinite), _ptr(underflow), n, _stream(stream)),
+           "fp8q_cast_multi_ex")
+
+
+def fp8q_loss_scaler_create(init_scale: float, growth_interval: int, min_scale: float = 1.0,
+                            max_scale: float = 2.0 ** 24) -> int:
+    h = ctypes.c_void_p()
+    _check(load().fp8q_loss_scaler_create(init_scale, growth_interval, min_scale, max_scale,
+                                          ctypes.byref(h)), "fp8q_loss_scaler_create")
+    return h.value
+
+
+def fp8q_loss_scaler_destroy(h: int):
+    _check(load().fp8q_loss_scaler_destroy(ctypes.c_void_p(h)), "fp8q_loss_scaler_destroy")
+
+
+def fp8q_loss_scaler_update(h: int, nonfinite: torch.Tensor, scale=None, skip=None, stream=None):
+    """nonfinite: int64 CUDA tensor of counts; scale: float32 CUDA scalar;
+    skip: int32 CUDA scalar."""
+    _check(load().fp8q_loss_scaler_update(ctypes.c_void_p(h), _ptr(nonfinite), nonfinite.numel(),
+                                          _ptr(scale), _ptr(skip), _stream(stream)),
+           "fp8q_loss_scaler_update")
+
+
+def fp8q_loss_scaler_read(h: int):
+    """(scale, clean-step streak)."""
+    sc, g = ctypes.c_float(), ctypes.c_int()
+    _check(load().fp8q_loss_scaler_read(ctypes.c_void_p(h), ctypes.byref(sc), ctypes.byref(g)),
+           "fp8q_loss_scaler_read")
+    return sc.value, g.value
 
 
 def mx_cast(x: torch.Tensor, fmt: int, headroom: int, q: torch.Tensor, e8m0: torch.Tensor,

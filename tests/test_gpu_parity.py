@@ -488,6 +488,109 @@ def test_estimator_resume_equals_continuous():
         g.close()
 
 
+def _counted_group_step(hs, xs, underflow=True):
+    n = len(hs)
+    qs = [torch.empty(x.numel(), dtype=torch.uint8, device="cuda") for x in xs]
+    outs = [torch.empty(n, dtype=torch.float32, device="cuda") for _ in range(2)]
+    cl = torch.empty(n, dtype=torch.int64, device="cuda")
+    nf = torch.full((n,), -1, dtype=torch.int64, device="cuda")
+    uf = torch.full((n,), -1, dtype=torch.int64, device="cuda") if underflow else None
+    F.fp8q_cast_multi_ex(hs, xs, qs, outs[0], outs[1], cl, nf, uf)
+    torch.cuda.synchronize()
+    return qs, outs, cl, nf, uf
+
+
+def test_nonfinite_and_underflow_counts():
+    """Per-tensor counts of NaN/Inf inputs and of finite nonzero inputs cast
+    to zero, against the oracle, for both formats and dtypes, sizes across
+    chunk boundaries; the bytes equal those of the launch without the
+    underflow count."""
+    rng = np.random.default_rng(61)
+    specs = [(f, dt, n) for f in (0, 1) for dt in (torch.bfloat16, torch.float32)
+             for n in (1, 100, 8193, 70001)]
+    hs = [F.fp8q_create(f, 2) for f, _, _ in specs]
+    hs2 = [F.fp8q_create(f, 2) for f, _, _ in specs]
+    orc = [policy.ScalingState(f, 2) for f, _, _ in specs]
+    for t in range(3):
+        xs = []
+        for i, (f, dt, n) in enumerate(specs):
+            v = rng.standard_normal(n) * np.exp(rng.uniform(-30, 3, n))
+            if n > 50:
+                v[rng.integers(0, n, 5)] = np.nan
+                v[rng.integers(0, n, 3)] = np.inf
+                v[rng.integers(0, n, 7)] = 0.0
+            xs.append(torch.from_numpy(v.astype(np.float32)).to(dt).cuda())
+        qs, outs, cl, nf, uf = _counted_group_step(hs, xs, True)
+        qs2, _, _, nf2, _ = _counted_group_step(hs2, xs, False)
+        for i, x in enumerate(xs):
+            q_o, a_o, s_o, c_o, _ = orc[i].step(host_bits(x), NT)
+            assert np.array_equal(qs[i].cpu().numpy(), q_o), (t, i)
+            assert torch.equal(qs[i], qs2[i])
+            nf_o, uf_o = coracle.count_special(host_bits(x), q_o)
+            assert (int(nf[i]), int(uf[i]), int(nf2[i])) == (nf_o, uf_o, nf_o), (t, i)
+    for h in hs + hs2:
+        F.fp8q_destroy(h)
+
+
+def test_underflow_count_full_size_gradients():
+    """Gradient-like tensors (magnitudes spread over 1e-8..1e2) underflow a
+    lot under E5M2 with a max-window scale: counts exact at full size."""
+    xs = synthetic.grad_group_step(2, "cuda")[:8]
+    hs = [F.fp8q_create(1, 16) for _ in xs]
+    orc = [policy.ScalingState(1, 16) for _ in xs]
+    for t in range(2):
+        qs, outs, cl, nf, uf = _counted_group_step(hs, xs, True)
+        for i, x in enumerate(xs):
+            q_o, *_ = orc[i].step(host_bits(x), NT)
+            assert np.array_equal(qs[i].cpu().numpy(), q_o.reshape(-1))
+            assert (int(nf[i]), int(uf[i])) == coracle.count_special(host_bits(x), q_o)
+    assert int(uf.sum()) > 0
+    for h in hs:
+        F.fp8q_destroy(h)
+
+
+def test_loss_scaler_against_oracle():
+    """The device loss scaler follows the oracle's state machine on a random
+    non-finite pattern, including the clamps."""
+    rng = np.random.default_rng(62)
+    for init, n, lo, hi in ((1024.0, 3, 1.0, 2.0 ** 24), (2.0 ** 23, 2, 1.0, 2.0 ** 24), (4.0, 1, 2.0, 64.0)):
+        ls = F.fp8q_loss_scaler_create(init, n, lo, hi)
+        o = policy.LossScaler(init, n, lo, hi)
+        scale = torch.empty(1, dtype=torch.float32, device="cuda")
+        skip = torch.empty(1, dtype=torch.int32, device="cuda")
+        for t in range(40):
+            counts = torch.from_numpy((rng.random(7) < 0.08).astype(np.int64) * rng.integers(1, 9, 7)).cuda()
+            F.fp8q_loss_scaler_update(ls, counts, scale, skip)
+            want_skip = o.update(counts.cpu().tolist())
+            torch.cuda.synchronize()
+            assert (float(scale.item()), bool(skip.item())) == (float(o.scale), want_skip), t
+        assert F.fp8q_loss_scaler_read(ls) == (float(o.scale), o.good)
+        F.fp8q_loss_scaler_destroy(ls)
+
+
+def test_loss_scaling_step_loop():
+    """Casts of gradient tensors feed their non-finite counts to the scaler
+    in one stream: an Inf in one tensor of a step halves the scale."""
+    hs = [F.fp8q_create(1, 4) for _ in range(3)]
+    ls = F.fp8q_loss_scaler_create(2.0 ** 16, 2)
+    o = policy.LossScaler(2.0 ** 16, 2)
+    scale = torch.empty(1, dtype=torch.float32, device="cuda")
+    skip = torch.empty(1, dtype=torch.int32, device="cuda")
+    for t in range(8):
+        xs = [torch.randn(5000, device="cuda") * 1e-3 for _ in hs]
+        if t in (2, 5):
+            xs[1][17] = float("inf")
+        qs, outs, cl, nf, uf = _counted_group_step(hs, xs, False)
+        F.fp8q_loss_scaler_update(ls, nf, scale, skip)
+        want = o.update(nf.cpu().tolist())
+        torch.cuda.synchronize()
+        assert bool(skip.item()) == want == (t in (2, 5))
+        assert float(scale.item()) == float(o.scale)
+    F.fp8q_loss_scaler_destroy(ls)
+    for h in hs:
+        F.fp8q_destroy(h)
+
+
 def test_per_tensor_error_stats():
     x = synthetic.spike_step(9, "cuda", shape=(1024, 1024))
     for fmt in (0, 1):
