@@ -41,7 +41,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="decoder",
-                   choices=["decoder", "current", "spike", "grad", "mx", "single"])
+                   choices=["decoder", "current", "spike", "grad", "mx", "transpose", "single"])
     p.add_argument("--n", type=int, default=1 << 26, help="elements for --workload single")
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-e2e", action="store_true")
@@ -194,8 +194,31 @@ class Workload:
             mx("mx_cast_nearest", x, 0, rule=2)
             mx("mx_cast_colwise_ocp", x, 0, axis=1)
             mx("mx_cast_colwise_ceil", x, 0, rule=1, axis=1)
+            r, c = x.shape
+            dq = [io_out((r, c), torch.uint8), io_out((r, c // 32), torch.uint8),
+                  io_out((c, r), torch.uint8), io_out((c, r // 32), torch.uint8)]
+            dcl = [torch.empty(1, dtype=torch.int64, device=dev) for _ in range(2)]
+            self.parts.append(Part("mx_cast_dual_ocp", "mx_dual_kernel",
+                                   x.numel() * (x.element_size() + 2) + 2 * (x.numel() // 32),
+                                   lambda k: F.mx_cast_dual(x, F.E4M3, 0, 0, *dq, *dcl),
+                                   lambda k: [x], lambda k: dq + dcl))
             self.name = ("MX E4M3 of bf16 [16384, 8192] tanh(N(0,2)): row-wise OCP, +1 headroom, "
-                         "ceil and nearest scale rules; column-wise OCP and ceil")
+                         "ceil and nearest scale rules; column-wise OCP and ceil; dual (row-wise + "
+                         "transposed column-wise) OCP")
+        elif kind == "transpose":
+            x = io_in(S.mx_tanh(dev))
+            r, c = x.shape
+            g = F.fp8q_create(F.E4M3, 16, 0, 0)
+            self.handles.append(g)
+            q, qt = io_out((r, c), torch.uint8), io_out((c, r), torch.uint8)
+            outs = torch.empty(3, dtype=torch.float32, device=dev)
+            self.parts.append(Part("cast_transpose", "cast_transpose_kernel",
+                                   x.numel() * (x.element_size() + 2),
+                                   lambda k: F.fp8q_cast_transpose(g, x, q, qt, outs[0:1], outs[1:2]),
+                                   lambda k: [x], lambda k: [q, qt]))
+            self.oracle_jobs.append(("cast", x, 0, 16, 0))
+            self.name = ("cast_transpose: bf16 [16384, 8192] -> E4M3 q [16384, 8192] and q^T "
+                         "[8192, 16384], max-window 16, one launch")
         elif kind == "spike":
             seq = [S.spike_step(s, dev) for s in range(S.SPIKE_STEPS)]
             for name, w, m in (("most_recent_w1", 1, 0), ("max_window_w16_m1", 16, 1)):
@@ -509,7 +532,7 @@ def run_ours(args, rank: int, world: int):
             "config": {"workload": W.name, "bytes_per_step": W.step_bytes,
                        "io": "bf16/fp32 in, FP8 (+E8M0) out",
                        "l2": f"inputs larger than L2 ({W.step_bytes / 1e9:.2f} GB moved per step)"
-                       if args.workload in ("decoder", "grad", "mx", "spike", "single")
+                       if args.workload in ("decoder", "grad", "mx", "spike", "single", "transpose")
                        else "tiny: L2-resident, latency only",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "kernel": dom.kernel, "achieved": dpart["GB/s"],

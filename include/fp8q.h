@@ -236,6 +236,30 @@ FP8Q_API int mx_cast_ex(const void* x, int dtype, int64_t rows, int64_t cols, in
                         int rule, int headroom_bits, int axis, uint8_t* q, uint8_t* e8m0,
                         unsigned long long* d_clipped, void* stream);
 
+/* Fused cast + transpose of a row-major [rows, cols] tensor with the
+ * handle's per-tensor scale: q [rows, cols] and its transpose qt [cols, rows]
+ * from one read of x, for matmuls that need both operands cast ("what
+ * actually breaks low precision training": real low-precision training casts
+ * both operands of the backward matmuls).  Scale, amax, clipped count and
+ * the history update are those of fp8q_cast on the same data (clipped
+ * elements are counted once).  rows and cols multiples of 32; x, q, qt
+ * 16-byte aligned.  One launch (plus the amax pre-pass under current
+ * scaling). */
+FP8Q_API int fp8q_cast_transpose(fp8q_handle h, const void* x, int dtype, int64_t rows, int64_t cols,
+                                 uint8_t* q, uint8_t* qt, float* d_scale_inv, float* d_amax,
+                                 unsigned long long* d_clipped, void* stream);
+
+/* MX dual cast: from one read of x [rows, cols], the row-wise MX cast
+ * (q_row [rows, cols], e8m0_row [rows, cols/32]) and the column-wise one
+ * written transposed, i.e. the row-wise MX cast of x^T (q_colt [cols, rows],
+ * e8m0_colt [cols, rows/32]).  Rule and headroom as mx_cast_ex.  rows and
+ * cols multiples of 32; x, q_row, q_colt 16-byte aligned.  d_clipped_row /
+ * d_clipped_col: device uint64 or NULL.  One launch (plus memsets). */
+FP8Q_API int mx_cast_dual(const void* x, int dtype, int64_t rows, int64_t cols, int format, int rule,
+                          int headroom_bits, uint8_t* q_row, uint8_t* e8m0_row, uint8_t* q_colt,
+                          uint8_t* e8m0_colt, unsigned long long* d_clipped_row,
+                          unsigned long long* d_clipped_col, void* stream);
+
 /* Read a handle's amax history (oldest first) to host memory.  Blocks until
  * the handle's last cast has finished.  capacity must be >= the window;
  * *n_valid receives the number of entries written. */

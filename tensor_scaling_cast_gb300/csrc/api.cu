@@ -113,7 +113,10 @@ FP8Q_API const char* fp8q_last_cuda_error(void) { return g_cuda_err; }
 
 FP8Q_API int fp8q_pipeline_status(unsigned int* timed_out_waits) {
   if (!timed_out_waits) return FP8Q_EINVAL;
-  cudaError_t e = read_wait_timeouts(timed_out_waits);
+  unsigned int a = 0, b = 0;
+  cudaError_t e = read_wait_timeouts(&a);
+  if (e == cudaSuccess) e = read_tp_wait_timeouts(&b);
+  *timed_out_waits = a + b;
   return e == cudaSuccess ? FP8Q_OK : fail_cuda(e);
 }
 
@@ -411,6 +414,83 @@ FP8Q_API int mx_cast_ex(const void* x, int dtype, int64_t rows, int64_t cols, in
                                           d_clipped, s, &launches);
   g_launches += launches;
   return e == cudaSuccess ? FP8Q_OK : fail_cuda(e);
+}
+
+FP8Q_API int mx_cast_dual(const void* x, int dtype, int64_t rows, int64_t cols, int format, int rule,
+                          int headroom_bits, uint8_t* q_row, uint8_t* e8m0_row, uint8_t* q_colt,
+                          uint8_t* e8m0_colt, unsigned long long* d_clipped_row,
+                          unsigned long long* d_clipped_col, void* stream) {
+  if (!dtype_ok(dtype) || !format_ok(format)) return FP8Q_EDTYPE;
+  if (rule < FP8Q_MX_FLOOR || rule > FP8Q_MX_NEAREST) return FP8Q_EINVAL;
+  if (rows < 0 || cols <= 0 || rows % 32 != 0 || cols % 32 != 0 || headroom_bits < 0 ||
+      headroom_bits > 4)
+    return FP8Q_EINVAL;
+  if (rows > 0 && cols > (int64_t(1) << 46) / rows) return FP8Q_EINVAL;
+  if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return FP8Q_EINVAL;
+  const int64_t n = rows * cols;
+  if (n > 0 && (!x || !q_row || !e8m0_row || !q_colt || !e8m0_colt)) return FP8Q_EINVAL;
+  if (!aligned16(x) || !aligned16(q_row) || !aligned16(q_colt)) return FP8Q_EALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  for (unsigned long long* c : {d_clipped_row, d_clipped_col}) {
+    if (!c) continue;
+    cudaError_t e = cudaMemsetAsync(c, 0, sizeof(unsigned long long), s);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  if (n == 0) return FP8Q_OK;
+  int launches = 0;
+  cudaError_t e = launch_mx_dual(x, dtype, rows, cols, format, rule, headroom_bits, q_row, e8m0_row,
+                                 q_colt, e8m0_colt, d_clipped_row, d_clipped_col, s, &launches);
+  g_launches += launches;
+  return e == cudaSuccess ? FP8Q_OK : fail_cuda(e);
+}
+
+FP8Q_API int fp8q_cast_transpose(fp8q_handle h, const void* x, int dtype, int64_t rows, int64_t cols,
+                                 uint8_t* q, uint8_t* qt, float* d_scale_inv, float* d_amax,
+                                 unsigned long long* d_clipped, void* stream) {
+  if (!handle_ok(h)) return FP8Q_EHANDLE;
+  if (!dtype_ok(dtype)) return FP8Q_EDTYPE;
+  if (rows <= 0 || cols <= 0 || rows % 32 != 0 || cols % 32 != 0) return FP8Q_EINVAL;
+  if (cols > (int64_t(1) << 46) / rows || rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31))
+    return FP8Q_EINVAL;
+  if (!x || !q || !qt) return FP8Q_EINVAL;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(qt)) return FP8Q_EALIGN;
+  int st = check_device(h);
+  if (st != FP8Q_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t n = rows * cols;
+  const bool current = h->estimator == FP8Q_EST_SMOOTHED ? h->host_casts == 0
+                                                         : (h->window == 0 || h->host_count == 0);
+  int launches = 0;
+  GroupHeader gh;
+  std::memset(&gh, 0, sizeof gh);
+  if (current) {
+    const int64_t ce = chunk_elems(dtype);
+    const long long nch = (n + ce - 1) / ce;
+    if (nch > 0x7FFFFFFFll) return FP8Q_EINVAL;
+    TensorDesc d;
+    d.x = x;
+    d.q = q;
+    d.n = n;
+    d.st = h->dev;
+    d.chunk_begin = 0;
+    d.flags = (dtype == FP8Q_BF16 ? 1 : 0) | (h->format == FP8Q_E5M2 ? 2 : 0) | (kCurrentPre << 2);
+    gh.total_chunks = (int32_t)nch;
+    cudaError_t e = launch_amax_group(gh, &d, 1, s, &launches);
+    g_launches += launches;
+    launches = 0;
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  gh.scale_inv = d_scale_inv;
+  gh.amax = d_amax;
+  gh.clipped = d_clipped;
+  gh.count = 1;
+  cudaError_t e = launch_cast_transpose(x, dtype, h->format, rows, cols, q, qt, h->dev,
+                                        current ? kCurrentPre : kDelayed, gh, s, &launches);
+  g_launches += launches;
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (h->window > 0 && h->host_count < h->window) h->host_count++;
+  h->host_casts++;
+  return record_last(h, s);
 }
 
 FP8Q_API int mx_cast(const void* x, int dtype, int64_t rows, int64_t cols, int format,

@@ -86,7 +86,15 @@ cudaError_t launch_stats(const void* x, int dtype, int64_t n, const uint8_t* q, 
                          const float* scale_inv, const uint8_t* e8m0, double* out,
                          cudaStream_t s, int* launches);
 
-cudaError_t read_wait_timeouts(unsigned int* count);   // and reset to 0
+cudaError_t read_wait_timeouts(unsigned int* count);      // and reset to 0 (mx.cu)
+cudaError_t read_tp_wait_timeouts(unsigned int* count);   // and reset to 0 (transpose.cu)
+cudaError_t launch_mx_dual(const void* x, int dtype, int64_t rows, int64_t cols, int format, int rule,
+                           int headroom, uint8_t* q_row, uint8_t* e8_row, uint8_t* q_colt,
+                           uint8_t* e8_colt, unsigned long long* cr, unsigned long long* cc,
+                           cudaStream_t s, int* launches);
+cudaError_t launch_cast_transpose(const void* x, int dtype, int format, int64_t rows, int64_t cols,
+                                  uint8_t* q, uint8_t* qt, DevState* st, int mode, const GroupHeader& h,
+                                  cudaStream_t s, int* launches);
 
 // Device state of a dynamic loss scaler.
 struct LossScaleState {

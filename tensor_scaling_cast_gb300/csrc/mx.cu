@@ -10,42 +10,13 @@
 // (leading-bit position for subnormals).  Blocks are independent, so there
 // is no cross-CTA step besides one atomic add of the clipped count.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "fp8q_device.cuh"
 #include "tma.cuh"
 #include "fp8q_internal.cuh"
 
 namespace fp8q {
-
-// Shared exponent of a block from its amax bits m (finite), per rule:
-//   floor (OCP): E = floor(log2 A) - emax_elem
-//   ceil:        smallest E with A * 2^-E <= fmax; with A = mu * 2^k this is
-//                k - emax_elem + [mu > 1.75]   (fmax = 1.75 * 2^emax_elem)
-//   nearest:     E nearest to log2(A / fmax):   k - emax_elem - [mu < 1.75/sqrt 2],
-//                tested exactly as M^2 < 49 * 2^41 on the 24-bit significand M
-// then + headroom, clamped to [-127, 127]; a zero block gets -127.
-template <int FMT>
-__device__ __forceinline__ int block_exp(uint32_t m, int rule, int headroom) {
-  if (m == 0u) return -127;
-  int k;
-  uint32_t M;
-  if (m >> 23) {
-    k = (int)(m >> 23) - 127;
-    M = 0x800000u | (m & 0x7FFFFFu);
-  } else {
-    const int lb = 31 - __clz((int)m);
-    k = lb - 149;
-    M = m << (23 - lb);
-  }
-  int E = k - emax_elem(FMT);
-  if (rule == FP8Q_MX_CEIL) E += (M > 0xE00000u) ? 1 : 0;
-  else if (rule == FP8Q_MX_NEAREST) E -= ((unsigned long long)M * M < (49ull << 41)) ? 1 : 0;
-  return min(127, max(-127, E + headroom));
-}
 
 template <int DT, int FMT>
 __global__ void __launch_bounds__(kThreads, 4) mx_kernel(const char* __restrict__ x, int64_t nelem,
@@ -338,22 +309,6 @@ __global__ void __launch_bounds__(kThreads, 2) mx_colwise_kernel(
   }
 }
 
-// cuTensorMapEncodeTiled from the driver, fetched through the runtime so the
-// library links no driver library of its own.
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult qr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
-            cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 template <int DT, int FMT>
 static cudaError_t launch_mx_col_t(const void* x, int64_t rows, int64_t cols, int headroom, int rule,
                                    uint8_t* q, uint8_t* e8m0, unsigned long long* clipped,
@@ -369,18 +324,9 @@ static cudaError_t launch_mx_col_t(const void* x, int64_t rows, int64_t cols, in
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, SMEM) != cudaSuccess || occ < 1)
       occ = 1;
   }
-  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-  if (!encode) return cudaErrorNotSupported;
   CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols * (DT == FP8Q_BF16 ? 2 : 4)};
-  const cuuint32_t box[2] = {(cuuint32_t)TILE_C, 32u};
-  const cuuint32_t estride[2] = {1u, 1u};
-  if (encode(&map, DT == FP8Q_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-             const_cast<void*>(x), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+  cudaError_t me = encode_tile_map(&map, x, DT == FP8Q_BF16, rows, cols, TILE_C);
+  if (me != cudaSuccess) return me;
   const int64_t ntiles = (rows / 32) * ((cols + TILE_C - 1) / TILE_C);
   long long grid = (long long)sm_count(device_of_current()) * occ;
   if (grid > ntiles) grid = ntiles;

@@ -63,6 +63,8 @@ def load() -> ctypes.CDLL:
     L.fp8q_loss_scaler_read.argtypes = [p, ctypes.POINTER(f), ctypes.POINTER(i)]
     L.mx_cast.argtypes = [p, i, i64, i64, i, i, p, p, p, p]
     L.mx_cast_ex.argtypes = [p, i, i64, i64, i, i, i, i, p, p, p, p]
+    L.mx_cast_dual.argtypes = [p, i, i64, i64, i, i, i, p, p, p, p, p, p, p]
+    L.fp8q_cast_transpose.argtypes = [p, p, i, i64, i64, p, p, p, p, p, p]
     L.fp8q_amax_history.argtypes = [p, ctypes.POINTER(f), i, ctypes.POINTER(i)]
     L.fp8q_scale_state.argtypes = [p, ctypes.POINTER(i), ctypes.POINTER(ctypes.c_longlong)]
     L.fp8q_set_history.argtypes = [p, ctypes.POINTER(f), i, i]
@@ -76,7 +78,7 @@ def load() -> ctypes.CDLL:
     L.fp8q_strerror.restype = ctypes.c_char_p
     L.fp8q_last_cuda_error.restype = ctypes.c_char_p
     L.fp8q_launch_count.restype = ctypes.c_longlong
-    for name in ("fp8q_cast_multi_ex", "fp8q_loss_scaler_create", "fp8q_loss_scaler_destroy",
+    for name in ("mx_cast_dual", "fp8q_cast_transpose", "fp8q_cast_multi_ex", "fp8q_loss_scaler_create", "fp8q_loss_scaler_destroy",
                  "fp8q_loss_scaler_update", "fp8q_loss_scaler_read",
                  "fp8q_create", "fp8q_create_ex", "fp8q_get_estimator_state",
                  "fp8q_set_estimator_state", "fp8q_destroy", "fp8q_cast", "fp8q_cast_multi", "mx_cast", "mx_cast_ex",
@@ -237,6 +239,26 @@ def mx_cast_ex(x: torch.Tensor, fmt: int, rule: int, headroom: int, axis: int, q
     rows, cols = x.shape
     _check(load().mx_cast_ex(_ptr(x), _dtype(x), rows, cols, fmt, rule, headroom, axis, _ptr(q),
                              _ptr(e8m0), _ptr(clipped), _stream(stream)), "mx_cast_ex")
+
+
+def mx_cast_dual(x: torch.Tensor, fmt: int, rule: int, headroom: int, q_row, e8_row, q_colt, e8_colt,
+                 clipped_row=None, clipped_col=None, stream=None):
+    """Row-wise MX of x and row-wise MX of x^T (column-wise blocks written
+    transposed) from one read: q_row [rows, cols], e8_row [rows, cols/32],
+    q_colt [cols, rows], e8_colt [cols, rows/32]."""
+    rows, cols = x.shape
+    _check(load().mx_cast_dual(_ptr(x), _dtype(x), rows, cols, fmt, rule, headroom, _ptr(q_row),
+                               _ptr(e8_row), _ptr(q_colt), _ptr(e8_colt), _ptr(clipped_row),
+                               _ptr(clipped_col), _stream(stream)), "mx_cast_dual")
+
+
+def fp8q_cast_transpose(h: int, x: torch.Tensor, q, qt, scale_inv=None, amax=None, clipped=None,
+                        stream=None):
+    """Per-tensor cast of x [rows, cols] to q [rows, cols] and qt [cols, rows]."""
+    rows, cols = x.shape
+    _check(load().fp8q_cast_transpose(ctypes.c_void_p(h), _ptr(x), _dtype(x), rows, cols, _ptr(q),
+                                      _ptr(qt), _ptr(scale_inv), _ptr(amax), _ptr(clipped),
+                                      _stream(stream)), "fp8q_cast_transpose")
 
 
 def fp8q_amax_history(h: int, capacity: int = MAX_WINDOW) -> list[float]:

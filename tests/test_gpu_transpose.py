@@ -1,0 +1,153 @@
+"""Parity of the fused cast + transpose kernels with the CPU oracle.
+
+fp8q_cast_transpose: q must equal the oracle's per-tensor cast of x and qt
+its transpose; amax, scale_inv, clipped and the history as for fp8q_cast.
+mx_cast_dual: (q_row, e8m0_row) must equal the oracle's row-wise MX cast of
+x and (q_colt, e8m0_colt) the row-wise MX cast of x^T.  All bit-exact.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import coracle, policy
+from tensor_scaling_cast_gb300 import fp8q as F
+from tensor_scaling_cast_gb300 import synthetic
+
+pytestmark = pytest.mark.gpu
+
+NT = os.cpu_count() or 1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA GPU is required for the gpu tests")
+    from tensor_scaling_cast_gb300 import build
+    build.build()
+    F.load()
+    torch.cuda.set_device(0)
+
+
+def host_bits(x: torch.Tensor) -> np.ndarray:
+    x = x.detach().contiguous().cpu()
+    if x.dtype == torch.bfloat16:
+        return x.view(torch.int16).numpy().view(np.uint16)
+    return x.view(torch.int32).numpy().view(np.uint32)
+
+
+def f32bits(t: torch.Tensor) -> int:
+    return int(t.detach().cpu().view(torch.int32).numpy().view(np.uint32).reshape(-1)[0])
+
+
+def _edge_tensor(rows, cols, dtype, seed):
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal((rows, cols)) * np.exp(rng.uniform(-30, 30, size=(rows, 1)))
+    v *= np.exp(rng.uniform(-10, 10, size=(1, cols)))
+    v[0:32, 0] = 0.0
+    v[0, :32] = 0.0
+    v[1, 7] = np.nan
+    v[40 % rows, 40 % cols] = -np.inf
+    v[3, :] *= 1e-38
+    v[4, cols // 2:] = 3e38
+    return torch.from_numpy(v.astype(np.float32)).to(dtype).cuda()
+
+
+def _dual_gpu(x, fmt, rule, headroom):
+    rows, cols = x.shape
+    qr = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+    er = torch.empty(rows, cols // 32, dtype=torch.uint8, device="cuda")
+    qc = torch.empty(cols, rows, dtype=torch.uint8, device="cuda")
+    ec = torch.empty(cols, rows // 32, dtype=torch.uint8, device="cuda")
+    cr = torch.empty(1, dtype=torch.int64, device="cuda")
+    cc = torch.empty(1, dtype=torch.int64, device="cuda")
+    F.mx_cast_dual(x, fmt, rule, headroom, qr, er, qc, ec, cr, cc)
+    torch.cuda.synchronize()
+    assert F.fp8q_pipeline_status() == 0
+    return [t.cpu().numpy() for t in (qr, er, qc, ec)] + [int(cr.item()), int(cc.item())]
+
+
+def _dual_oracle(xb, fmt, rule, headroom, nthreads=1):
+    qr, er, cr = coracle.mx_cast_ex(xb, fmt, rule, headroom, 0, nthreads)
+    qc, ec, cc = coracle.mx_cast_ex(np.ascontiguousarray(xb.T), fmt, rule, headroom, 0, nthreads)
+    return qr, er, qc, ec, cr, cc
+
+
+@pytest.mark.parametrize("rule", [0, 1, 2])
+def test_mx_dual_full_size(rule):
+    """bf16 [16384, 8192] tanh(N(0,2)) -> both MX E4M3 layouts in one pass."""
+    x = synthetic.mx_tanh("cuda")
+    got = _dual_gpu(x, 0, rule, 0)
+    want = _dual_oracle(host_bits(x), 0, rule, 0, NT)
+    names = ["q_row", "e8m0_row", "q_colt", "e8m0_colt"]
+    for g, w, nm in zip(got[:4], want[:4], names):
+        assert np.array_equal(g, w), nm
+    assert got[4:] == list(want[4:])
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_mx_dual_edge_values(dtype):
+    """Zero / NaN / Inf / subnormal / huge blocks, ragged column tiles,
+    both formats, every rule, headroom 0 and 2."""
+    for rows, cols in ((96, 320), (32, 32), (64, 288)):
+        x = _edge_tensor(rows, cols, dtype, rows * 7 + cols)
+        xb = host_bits(x)
+        for fmt in (0, 1):
+            for rule in (0, 1, 2):
+                for h in (0, 2):
+                    got = _dual_gpu(x, fmt, rule, h)
+                    want = _dual_oracle(xb, fmt, rule, h)
+                    for g, w in zip(got[:4], want[:4]):
+                        assert np.array_equal(g, w), (rows, cols, fmt, rule, h)
+                    assert got[4:] == list(want[4:]), (rows, cols, fmt, rule, h)
+
+
+def _ct_steps(shape, dtype, fmt, window, steps, make):
+    rows, cols = shape
+    h = F.fp8q_create(fmt, window, 1 if window else 0)
+    o = policy.ScalingState(fmt, window, 1 if window else 0)
+    for t in range(steps):
+        x = make(t)
+        q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+        qt = torch.empty(cols, rows, dtype=torch.uint8, device="cuda")
+        outs = torch.empty(2, dtype=torch.float32, device="cuda")
+        cl = torch.empty(1, dtype=torch.int64, device="cuda")
+        F.fp8q_cast_transpose(h, x, q, qt, outs[0:1], outs[1:2], cl)
+        torch.cuda.synchronize()
+        q_o, a_o, s_o, c_o, _ = o.step(host_bits(x).reshape(-1), NT)
+        q_o = q_o.reshape(rows, cols)
+        assert np.array_equal(q.cpu().numpy(), q_o), t
+        assert np.array_equal(qt.cpu().numpy(), q_o.T), t
+        assert (f32bits(outs[0:1]), f32bits(outs[1:2]), int(cl.item())) == (s_o, a_o, c_o), t
+    assert F.fp8q_pipeline_status() == 0
+    hist = F.fp8q_amax_history(h, max(1, window))
+    assert [np.float32(v).view(np.uint32) for v in hist] == o.hist
+    F.fp8q_destroy(h)
+
+
+@pytest.mark.parametrize("window", [0, 1, 16])
+def test_cast_transpose_spike_sequence(window):
+    """bf16 [4096, 4096] spike sequence (x8 at step 9): q and q^T each step,
+    current scaling (pre-pass) on step 0 or every step."""
+    _ct_steps((4096, 4096), torch.bfloat16, 0, window, 12,
+              lambda t: synthetic.spike_step(t, "cuda"))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_cast_transpose_edge_values(dtype, fmt):
+    for shape in ((96, 320), (32, 32), (64, 288)):
+        _ct_steps(shape, dtype, fmt, 2, 3,
+                  lambda t, shape=shape: _edge_tensor(shape[0], shape[1], dtype, 100 * t + shape[1]) * (4.0 ** t))
+
+
+def test_cast_transpose_argument_checks():
+    h = F.fp8q_create(0, 4)
+    x = torch.zeros(48, 64, dtype=torch.bfloat16, device="cuda")
+    q = torch.empty(48, 64, dtype=torch.uint8, device="cuda")
+    qt = torch.empty(64, 48, dtype=torch.uint8, device="cuda")
+    with pytest.raises(F.Fp8qError) as ei:
+        F.fp8q_cast_transpose(h, x, q, qt)             # rows not a multiple of 32
+    assert ei.value.status == -1
+    F.fp8q_destroy(h)
