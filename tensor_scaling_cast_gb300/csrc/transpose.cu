@@ -90,6 +90,71 @@ __device__ __forceinline__ void store32(uint8_t* dst, const uint32_t (&o)[8]) {
   __stcs(reinterpret_cast<uint4*>(dst) + 1, make_uint4(o[4], o[5], o[6], o[7]));
 }
 
+// bf16 column pairs: a 32-bit shared word holds columns 2p (low half) and
+// 2p + 1 (high half) of one row, so a pair costs one load per row.
+template <int HI>
+__device__ __forceinline__ uint32_t half_bits(uint32_t w) {
+  return HI ? (w & 0xFFFF0000u) : (w << 16);
+}
+
+template <int FMT, int HI>
+__device__ __forceinline__ void cast32_half(const uint32_t (&w)[32], float s, uint32_t (&o)[8]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t lo = cvt_pair<FMT>(__uint_as_float(half_bits<HI>(w[4 * k])) * s,
+                                      __uint_as_float(half_bits<HI>(w[4 * k + 1])) * s);
+    const uint32_t hi = cvt_pair<FMT>(__uint_as_float(half_bits<HI>(w[4 * k + 2])) * s,
+                                      __uint_as_float(half_bits<HI>(w[4 * k + 3])) * s);
+    o[k] = lo | (hi << 16);
+  }
+}
+
+__device__ __forceinline__ void load_pair_column(const uint4* tile, int p, uint32_t (&w)[32]) {
+  const uint32_t* t32 = reinterpret_cast<const uint32_t*>(tile);
+#pragma unroll
+  for (int r = 0; r < 32; ++r) w[r] = t32[r * 128 + p];
+}
+
+// One MX column block (half HI of a bf16 column pair): E8M0 byte, 32 bytes.
+template <int FMT, int HI>
+__device__ __forceinline__ void mx_column_half(const uint32_t (&w)[32], uint32_t m, int rule, int headroom,
+                                               uint32_t& clip, uint8_t* dst, uint8_t* e8dst) {
+  uint32_t o[8];
+  uint32_t ebyte;
+  if (m >= 0x7F800000u) {
+    ebyte = 0xFFu;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) set_byte(o, k, ((half_bits<HI>(w[k]) >> 31) << 7) | 0x7Fu);
+  } else {
+    const int E = block_exp<FMT>(m, rule, headroom);
+    ebyte = (uint32_t)(E + 127);
+    const float s = __uint_as_float((uint32_t)(127 - E) << 23);
+    cast32_half<FMT, HI>(w, s, o);
+    const int be = (int)(fmax_bits(FMT) >> 23) + E;
+    if (be < 255 && m > fmax_bits(FMT) + ((uint32_t)E << 23)) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) clip += clips<FMT>(__uint_as_float(half_bits<HI>(w[k])) * s) ? 1u : 0u;
+    }
+  }
+  store32(dst, o);
+  *e8dst = (uint8_t)ebyte;
+}
+
+// One per-tensor column (half HI of a bf16 column pair) with scale s.
+template <int FMT, int HI>
+__device__ __forceinline__ void ct_column_half(const uint32_t (&w)[32], uint32_t m, float s, uint8_t* dst) {
+  uint32_t o[8];
+  cast32_half<FMT, HI>(w, s, o);
+  if (m > 0x7F800000u) {                                 // a NaN in the column
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const uint32_t b = half_bits<HI>(w[k]);
+      if ((b & 0x7FFFFFFFu) > 0x7F800000u) set_byte(o, k, ((b >> 31) << 7) | 0x7Fu);
+    }
+  }
+  store32(dst, o);
+}
+
 // Shared pipeline bookkeeping of both kernels: this CTA's tiles are
 // blockIdx.x + j * gridDim.x; thread 0 keeps kTpStages - 1 tiles in flight.
 struct TilePipe {
@@ -214,7 +279,20 @@ __global__ void __launch_bounds__(kTpThreads, 2) mx_dual_kernel(
     }
 
     // B. column-wise blocks, written transposed
-    if (tid < TILE_C && c0 + tid < cols) {
+    if (DT == FP8Q_BF16) {
+      if (tid < TILE_C / 2 && c0 + 2 * tid < cols) {      // one bf16 column pair per thread
+        uint32_t w[32];
+        load_pair_column(tile, tid, w);
+        uint32_t pm = 0;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) pm = vmax_u16x2(pm, w[k] & 0x7FFF7FFFu);
+        const int64_t c = c0 + 2 * tid;
+        mx_column_half<FMT, 0>(w, pm << 16, rule, headroom, clip_c, q_colt + c * rows + r0,
+                               e8_colt + c * rb + (r0 >> 5));
+        mx_column_half<FMT, 1>(w, pm & 0xFFFF0000u, rule, headroom, clip_c,
+                               q_colt + (c + 1) * rows + r0, e8_colt + (c + 1) * rb + (r0 >> 5));
+      }
+    } else if (tid < TILE_C && c0 + tid < cols) {
       uint32_t b[32];
       load_column<DT>(tile, tid, b);
       uint32_t m = 0;
@@ -308,8 +386,19 @@ __global__ void __launch_bounds__(kTpThreads, 2) cast_transpose_kernel(
         else __stcs(reinterpret_cast<unsigned int*>(dst), out.x);
       }
     }
-    // B. transposed: one thread per column (clipping was counted in A)
-    if (tid < TILE_C && c0 + tid < cols) {
+    // B. transposed (clipping was counted in A)
+    if (DT == FP8Q_BF16) {
+      if (tid < TILE_C / 2 && c0 + 2 * tid < cols) {      // one bf16 column pair per thread
+        uint32_t w[32];
+        load_pair_column(tile, tid, w);
+        uint32_t pm = 0;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) pm = vmax_u16x2(pm, w[k] & 0x7FFF7FFFu);
+        const int64_t c = c0 + 2 * tid;
+        ct_column_half<FMT, 0>(w, pm << 16, s, qt + c * rows + r0);
+        ct_column_half<FMT, 1>(w, pm & 0xFFFF0000u, s, qt + (c + 1) * rows + r0);
+      }
+    } else if (tid < TILE_C && c0 + tid < cols) {
       uint32_t b[32];
       load_column<DT>(tile, tid, b);
       uint32_t o[8];
