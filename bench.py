@@ -501,6 +501,7 @@ def run_ours(args, rank: int, world: int):
     dom = max(W.parts, key=lambda p: parts[p.name]["ms"])
     dpart = parts[dom.name]
 
+    copy_ref = copy_reference(dev, W.step_bytes)
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(W, args.e2e_steps, world, dev, warm + K)
@@ -535,6 +536,7 @@ def run_ours(args, rank: int, world: int):
                        if args.workload in ("decoder", "grad", "mx", "spike", "single", "transpose")
                        else "tiny: L2-resident, latency only",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
+            "frac_of_same_box_copy": round(dpart["GB/s"] / copy_ref["GB/s"], 4),
             "roofline": {"bound": "hbm", "kernel": dom.kernel, "achieved": dpart["GB/s"],
                          "peak": peak, "unit": "GB/s", "frac": dpart["frac"],
                          "peak_source": "measured: MEASURED_PEAKS.json hbm_gbs (copy)"
@@ -543,6 +545,7 @@ def run_ours(args, rank: int, world: int):
                          "traffic": captured_traffic() if (args.workload == "decoder"
                                                            and dom.kernel == "cast_group_kernel") else None},
             "parts": parts,
+            "copy_reference": copy_ref,
             "gpu_launches": launches,
             "clocks": clk,
             "e2e": e2e,
@@ -551,6 +554,31 @@ def run_ours(args, rank: int, world: int):
         if args.workload == "current":
             line["latency_us_per_cast"] = round(ms_step * 1e3, 2)
         print(json.dumps(line), flush=True)
+
+
+def copy_reference(dev, step_bytes: int):
+    """Device-to-device copy on this GPU, timed the same way: the
+    achievable-copy figure for this box (read + write bytes / time), and
+    the dominant kernel's rate as a fraction of it."""
+    import torch
+    n = min(1 << 30, max(1 << 26, step_bytes // 4)) // 2      # bf16 elements per buffer
+    a = torch.empty(n, dtype=torch.bfloat16, device=dev).fill_(1.0)
+    b = torch.empty_like(a)
+    for _ in range(3):
+        b.copy_(a)
+    torch.cuda.synchronize()
+    reps = 20
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        b.copy_(a)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    gbs = 2 * a.numel() * 2 / (ms * 1e-3) / 1e9
+    del a, b
+    torch.cuda.empty_cache()
+    return {"GB/s": round(gbs, 1), "bytes": 4 * n, "how": "torch copy_ of a bf16 buffer, mean of 20"}
 
 
 def run_e2e_zero_copy(args, world: int, dev):
