@@ -34,6 +34,33 @@ int device_of_current() {
   return d;
 }
 
+// Resident CTAs per SM of a kernel at `threads` threads and `smem` bytes of
+// dynamic shared memory, computed once per (kernel, size, device); the
+// kernel's dynamic shared-memory limit is raised to `smem` first when that
+// exceeds the 48 KiB default.  Thread-safe.
+cudaError_t kernel_occupancy(const void* kernel, int threads, int smem, int* occ) {
+  struct Entry { const void* k; int threads, smem, device, occ; };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  const int device = device_of_current();
+  std::lock_guard<std::mutex> lk(mu);
+  for (const Entry& en : cache)
+    if (en.k == kernel && en.threads == threads && en.smem == smem && en.device == device) {
+      *occ = en.occ;
+      return cudaSuccess;
+    }
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  int v = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, threads, (size_t)smem) != cudaSuccess || v < 1)
+    v = 1;
+  cache.push_back({kernel, threads, smem, device, v});
+  *occ = v;
+  return cudaSuccess;
+}
+
 int sm_count(int device) {
   static std::mutex mu;
   static int cache[128] = {0};

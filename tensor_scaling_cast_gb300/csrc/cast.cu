@@ -273,14 +273,6 @@ __global__ void __launch_bounds__(kThreads, 4) amax_group_kernel(const __grid_co
 
 // ---- host-side launch ------------------------------------------------------
 
-template <typename K>
-static int resident_ctas(K kernel) {
-  int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0) != cudaSuccess || nb < 1)
-    nb = 1;
-  return nb;
-}
-
 template <int MAXT, int KIND>   // KIND 0: amax pre-pass, 1: cast, 2: cast + underflow count
 static cudaError_t launch_group_t(const GroupHeader& h, const TensorDesc* d, int count,
                                   cudaStream_t s, int* launches) {
@@ -290,8 +282,9 @@ static cudaError_t launch_group_t(const GroupHeader& h, const TensorDesc* d, int
   for (int i = 0; i < count; ++i) p.d[i] = d[i];
   auto kern = KIND == 0 ? amax_group_kernel<MAXT>
                         : (KIND == 1 ? cast_group_kernel<MAXT, false> : cast_group_kernel<MAXT, true>);
-  static int occ = 0;
-  if (occ == 0) occ = resident_ctas(kern);
+  int occ = 1;
+  cudaError_t oe = kernel_occupancy(reinterpret_cast<const void*>(kern), kThreads, 0, &occ);
+  if (oe != cudaSuccess) return oe;
   const int dev = device_of_current();
   long long grid = (long long)sm_count(dev) * occ;
   if (grid > h.total_chunks) grid = h.total_chunks;

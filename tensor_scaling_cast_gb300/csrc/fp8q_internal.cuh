@@ -106,6 +106,7 @@ cudaError_t launch_loss_scale_update(LossScaleState* st, const unsigned long lon
                                      float* scale_out, int* skip_out, cudaStream_t s, int* launches);
 
 int sm_count(int device);
+cudaError_t kernel_occupancy(const void* kernel, int threads, int smem, int* occ);
 int record_cuda_error(cudaError_t e);   // keeps the text, returns FP8Q_ECUDA
 void note_launches(int k);              // adds to fp8q_launch_count()
 int device_of_current();

@@ -95,11 +95,9 @@ static cudaError_t launch_mx_t(const void* x, int64_t nelem, int headroom, int r
                                int* launches) {
   constexpr int EPL = DT == FP8Q_BF16 ? 8 : 4;
   constexpr int64_t TILE = (int64_t)kThreads * kUnroll * EPL;
-  static int occ = 0;
-  if (occ == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, mx_kernel<DT, FMT>, kThreads, 0) != cudaSuccess || occ < 1)
-      occ = 1;
-  }
+  int occ = 1;
+  cudaError_t oe = kernel_occupancy(reinterpret_cast<const void*>(mx_kernel<DT, FMT>), kThreads, 0, &occ);
+  if (oe != cudaSuccess) return oe;
   const int64_t ntiles = (nelem + TILE - 1) / TILE;
   long long grid = (long long)sm_count(device_of_current()) * occ;
   if (grid > ntiles) grid = ntiles;
@@ -317,13 +315,9 @@ static cudaError_t launch_mx_col_t(const void* x, int64_t rows, int64_t cols, in
   constexpr int TILE_C = 32 * EPL;
   constexpr int SMEM = kColStages * kColTileBytes + 1024;
   auto kern = mx_colwise_kernel<DT, FMT>;
-  static int occ = 0;
-  if (occ == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-    if (e != cudaSuccess) return e;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, SMEM) != cudaSuccess || occ < 1)
-      occ = 1;
-  }
+  int occ = 1;
+  cudaError_t oe = kernel_occupancy(reinterpret_cast<const void*>(kern), kThreads, SMEM, &occ);
+  if (oe != cudaSuccess) return oe;
   CUtensorMap map;
   cudaError_t me = encode_tile_map(&map, x, DT == FP8Q_BF16, rows, cols, TILE_C);
   if (me != cudaSuccess) return me;

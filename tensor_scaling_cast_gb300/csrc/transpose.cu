@@ -437,18 +437,6 @@ __global__ void __launch_bounds__(kTpThreads, 2) cast_transpose_kernel(
 // launches
 // ---------------------------------------------------------------------------
 
-template <typename K>
-static cudaError_t prepare(K kern, int* occ) {
-  constexpr int SMEM = kTpStages * kTpTileBytes + 1024;
-  if (*occ == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-    if (e != cudaSuccess) return e;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kern, kTpThreads, SMEM) != cudaSuccess || *occ < 1)
-      *occ = 1;
-  }
-  return cudaSuccess;
-}
-
 template <int DT, int FMT>
 static cudaError_t launch_dual_t(const void* x, int64_t rows, int64_t cols, int rule, int headroom,
                                  uint8_t* q_row, uint8_t* e8_row, uint8_t* q_colt, uint8_t* e8_colt,
@@ -456,8 +444,9 @@ static cudaError_t launch_dual_t(const void* x, int64_t rows, int64_t cols, int 
                                  int* launches) {
   constexpr int TILE_C = TileGeom<DT>::TILE_C;
   auto kern = mx_dual_kernel<DT, FMT>;
-  static int occ = 0;
-  cudaError_t e = prepare(kern, &occ);
+  int occ = 1;
+  cudaError_t e = kernel_occupancy(reinterpret_cast<const void*>(kern), kTpThreads,
+                                   kTpStages * kTpTileBytes + 1024, &occ);
   if (e != cudaSuccess) return e;
   CUtensorMap map;
   e = encode_tile_map(&map, x, DT == FP8Q_BF16, rows, cols, TILE_C);
@@ -491,8 +480,9 @@ static cudaError_t launch_ct_t(const void* x, int64_t rows, int64_t cols, uint8_
                                int* launches) {
   constexpr int TILE_C = TileGeom<DT>::TILE_C;
   auto kern = cast_transpose_kernel<DT, FMT>;
-  static int occ = 0;
-  cudaError_t e = prepare(kern, &occ);
+  int occ = 1;
+  cudaError_t e = kernel_occupancy(reinterpret_cast<const void*>(kern), kTpThreads,
+                                   kTpStages * kTpTileBytes + 1024, &occ);
   if (e != cudaSuccess) return e;
   CUtensorMap map;
   e = encode_tile_map(&map, x, DT == FP8Q_BF16, rows, cols, TILE_C);
