@@ -502,6 +502,7 @@ def run_ours(args, rank: int, world: int):
     dpart = parts[dom.name]
 
     copy_ref = copy_reference(dev, W.step_bytes)
+    results = workload_results(args.workload, dev) if rank == 0 else None
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(W, args.e2e_steps, world, dev, warm + K)
@@ -553,7 +554,90 @@ def run_ours(args, rank: int, world: int):
         }
         if args.workload == "current":
             line["latency_us_per_cast"] = round(ms_step * 1e3, 2)
+        if results is not None:
+            line["results"] = results
         print(json.dumps(line), flush=True)
+
+
+def workload_results(kind: str, dev):
+    """The quantities each configuration asks to report, computed with the
+    library on fresh handles outside the timed region."""
+    import torch
+
+    from tensor_scaling_cast_gb300 import fp8q as F
+    from tensor_scaling_cast_gb300 import synthetic as S
+
+    def f32(t):
+        return float(t.item())
+
+    if kind == "current":
+        x = S.current_4096(dev)
+        g = F.ScaledCast(F.E4M3, 0, 0)
+        q, sinv, amax, clipped = g(x)
+        g.close()
+        return {"amax": f32(amax), "scale": 1.0 / f32(sinv), "scale_inv": f32(sinv),
+                "clipped": int(clipped.item()), "fp8_bytes_head": q[:8].cpu().tolist()}
+    if kind == "spike":
+        seq = [S.spike_step(t, dev) for t in range(S.SPIKE_STEPS)]
+        n = seq[0].numel()
+        out = {}
+        for name, kw in (("most_recent_w1", dict(window=1)),
+                         ("max_window_w16_m1", dict(window=16, margin=1)),
+                         ("smoothed_a0.1", dict(window=0, estimator=1, alpha=0.1)),
+                         ("smoothed_a0.5", dict(window=0, estimator=1, alpha=0.5)),
+                         ("max_window_w16_interval4", dict(window=16, interval=4))):
+            g = F.ScaledCast(F.E4M3, **kw)
+            fr = []
+            for x in seq:
+                _, _, _, c = g(x)
+                fr.append(int(c.item()) / n)
+            g.close()
+            out[name] = [round(v, 7) for v in fr]
+        return {"clipped_fraction_per_step": out, "spike_step": S.SPIKE_STEP}
+    if kind in ("mx", "transpose"):
+        if kind == "transpose":
+            return None
+        x = S.mx_tanh(dev)
+        r, c = x.shape
+        out = {}
+        for name, rule, h, axis in (("ocp", 0, 0, 0), ("headroom1", 0, 1, 0), ("ceil", 1, 0, 0),
+                                    ("nearest", 2, 0, 0), ("colwise_ocp", 0, 0, 1)):
+            q = torch.empty(r, c, dtype=torch.uint8, device=dev)
+            e8 = torch.empty((r, c // 32) if axis == 0 else (r // 32, c), dtype=torch.uint8, device=dev)
+            cl = torch.empty(1, dtype=torch.int64, device=dev)
+            F.mx_cast_ex(x, F.E4M3, rule, h, axis, q, e8, cl)
+            entry = {"clipped_fraction": int(cl.item()) / x.numel()}
+            if axis == 0:
+                st = torch.empty(3, dtype=torch.float64, device=dev)
+                F.mx_error_stats(x, q, e8, F.E4M3, st)
+                mse, bias, _ = st.cpu().tolist()
+                entry.update(mse=mse, bias=bias)
+            out[name] = entry
+        return {"mx_e4m3": out}
+    if kind in ("grad", "decoder"):
+        if kind == "grad":
+            xs = S.grad_group_step(1, dev)
+            fmts = [F.E5M2] * len(xs)
+        else:
+            specs = S.decoder_tensor_specs()[:16]            # layer 0
+            xs = [S.decoder_tensor(sp, 0, dev) for sp in specs]
+            fmts = [sp[2] for sp in specs]
+        hs = [F.fp8q_create(f, 16) for f in fmts]
+        m = len(xs)
+        res = []
+        for step in range(2):
+            qs = [torch.empty(x.numel(), dtype=torch.uint8, device=dev) for x in xs]
+            cl, nf, uf = (torch.empty(m, dtype=torch.int64, device=dev) for _ in range(3))
+            F.fp8q_cast_multi_ex(hs, xs, qs, None, None, cl, nf, uf)
+            ntot = sum(x.numel() for x in xs)
+            res.append({"clipped_fraction": int(cl.sum()) / ntot, "underflow_fraction": int(uf.sum()) / ntot,
+                        "nonfinite": int(nf.sum())})
+            del qs
+        for h in hs:
+            F.fp8q_destroy(h)
+        scope = "64 gradient tensors" if kind == "grad" else "layer 0 (16 tensors)"
+        return {"scope": scope, "step0_current_scaling": res[0], "step1_max_window": res[1]}
+    return None
 
 
 def copy_reference(dev, step_bytes: int):

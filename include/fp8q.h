@@ -328,6 +328,12 @@ FP8Q_API int fp8q_error_stats_noalloc(const void* x, int dtype, int64_t n, const
  * healthy run reads 0.  Synchronous. */
 FP8Q_API int fp8q_pipeline_status(unsigned int* timed_out_waits);
 
+/* Diagnostic of the timeout path: one CTA waits on a pipeline barrier that
+ * nothing completes.  Its bounded wait gives up (after about half a second)
+ * and is counted, so fp8q_pipeline_status reports one more timed-out wait;
+ * the device stays usable.  One launch. */
+FP8Q_API int fp8q_pipeline_selftest(void* stream);
+
 /* Name of a status code (static string). */
 FP8Q_API const char* fp8q_strerror(int code);
 

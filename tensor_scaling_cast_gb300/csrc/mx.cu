@@ -342,6 +342,26 @@ cudaError_t launch_mx_colwise(const void* x, int dtype, int64_t rows, int64_t co
              : launch_mx_col_t<FP8Q_F32, FP8Q_E5M2>(x, rows, cols, headroom, rule, q, e8m0, clipped, s, launches);
 }
 
+// Diagnostic: one warp waits on a barrier that nothing arms or completes.
+// The bounded wait gives up at its deadline and the timeout is counted, as
+// a stalled tile would be; nothing faults and nothing spins without end.
+__global__ void pipeline_selftest_kernel() {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait(&bar, 0u);
+  if (__syncthreads_or(!ok) && threadIdx.x == 0) atomicAdd(&g_wait_timeouts, 1u);
+}
+
+cudaError_t launch_pipeline_selftest(cudaStream_t s, int* launches) {
+  pipeline_selftest_kernel<<<1, 32, 0, s>>>();
+  ++*launches;
+  return cudaGetLastError();
+}
+
 cudaError_t read_wait_timeouts(unsigned int* count) {
   unsigned int zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(unsigned int));

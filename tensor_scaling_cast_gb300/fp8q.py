@@ -74,6 +74,8 @@ def load() -> ctypes.CDLL:
     L.fp8q_error_stats_noalloc.argtypes = [p, i, i64, p, i, p, p, p]
     L.fp8q_pipeline_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     L.fp8q_pipeline_status.restype = i
+    L.fp8q_pipeline_selftest.argtypes = [p]
+    L.fp8q_pipeline_selftest.restype = i
     L.fp8q_strerror.argtypes = [i]
     L.fp8q_strerror.restype = ctypes.c_char_p
     L.fp8q_last_cuda_error.restype = ctypes.c_char_p
@@ -120,6 +122,11 @@ def fp8q_pipeline_status() -> int:
     n = ctypes.c_uint()
     _check(load().fp8q_pipeline_status(ctypes.byref(n)), "fp8q_pipeline_status")
     return n.value
+
+
+def fp8q_pipeline_selftest(stream=None):
+    """Launch the never-completed barrier wait (see the C header)."""
+    _check(load().fp8q_pipeline_selftest(_stream(stream)), "fp8q_pipeline_selftest")
 
 
 def launch_count() -> int:

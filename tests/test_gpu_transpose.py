@@ -151,3 +151,20 @@ def test_cast_transpose_argument_checks():
         F.fp8q_cast_transpose(h, x, q, qt)             # rows not a multiple of 32
     assert ei.value.status == -1
     F.fp8q_destroy(h)
+
+
+def test_pipeline_wait_gives_up_and_is_reported():
+    """A barrier wait that nothing completes ends at its deadline, is counted
+    by fp8q_pipeline_status, and leaves the device usable."""
+    import time
+    F.fp8q_pipeline_status()                          # clear
+    t0 = time.time()
+    F.fp8q_pipeline_selftest()
+    torch.cuda.synchronize()
+    assert 0.05 < time.time() - t0 < 30
+    assert F.fp8q_pipeline_status() == 1
+    assert F.fp8q_pipeline_status() == 0              # read resets
+    x = synthetic.mx_tanh("cuda", shape=(64, 256))
+    got = _dual_gpu(x, 0, 0, 0)
+    want = _dual_oracle(host_bits(x), 0, 0, 0)
+    assert all(np.array_equal(g, w) for g, w in zip(got[:4], want[:4]))
