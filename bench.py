@@ -505,15 +505,27 @@ def run_ours(args, rank: int, world: int):
     results = workload_results(args.workload, dev) if rank == 0 else None
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(W, args.e2e_steps, world, dev, warm + K)
-        if hasattr(torch._C, "_host_emptyCache"):
-            torch._C._host_emptyCache()          # give the staging mirrors back
-        if args.workload in ("decoder", "grad", "mx", "single"):
+        need = pinned_bytes(W)
+        ok, why = host_memory_allows(need)
+        zero_copy_ok = args.workload in ("decoder", "grad", "mx", "single", "transpose")
+        if not ok:
+            e2e = {"value": None, "skipped": why}
+        elif world > 1 and zero_copy_ok:
+            # one pinned copy of the workload per rank: the zero-copy path only
             zc = run_e2e_zero_copy(args, world, dev)
-            e2e["staged_copy"] = {k: e2e[k] for k in ("value", "ms_per_step", "phases_ms", "path")}
-            e2e["zero_copy"] = zc
-            if zc["value"] > e2e["value"]:
-                e2e.update(value=zc["value"], ms_per_step=zc["ms_per_step"], path=zc["path"])
+            h2d = sum(t.numel() * t.element_size() for p in W.parts for t in p.inputs(0))
+            d2h = sum(t.numel() * t.element_size() for p in W.parts for t in p.outputs(0))
+            e2e = dict(zc, h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h)
+        else:
+            e2e = run_e2e(W, args.e2e_steps, world, dev, warm + K)
+            if hasattr(torch._C, "_host_emptyCache"):
+                torch._C._host_emptyCache()          # give the staging mirrors back
+            if zero_copy_ok:
+                zc = run_e2e_zero_copy(args, world, dev)
+                e2e["staged_copy"] = {k: e2e[k] for k in ("value", "ms_per_step", "phases_ms", "path")}
+                e2e["zero_copy"] = zc
+                if zc["value"] > e2e["value"]:
+                    e2e.update(value=zc["value"], ms_per_step=zc["ms_per_step"], path=zc["path"])
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -663,6 +675,32 @@ def copy_reference(dev, step_bytes: int):
     del a, b
     torch.cuda.empty_cache()
     return {"GB/s": round(gbs, 1), "bytes": 4 * n, "how": "torch copy_ of a bf16 buffer, mean of 20"}
+
+
+def pinned_bytes(W) -> int:
+    """Host bytes one pinned copy of a step's inputs and outputs takes."""
+    seen, total = set(), 0
+    for p in W.parts:
+        for t in list(p.inputs(0)) + list(p.outputs(0)):
+            if id(t) not in seen:
+                seen.add(id(t))
+                total += t.numel() * t.element_size()
+    return total
+
+
+def host_memory_allows(need: int):
+    """True when this rank's share of the available host memory (shared by
+    the ranks on this node) holds `need` bytes with a 25% margin."""
+    try:
+        avail = os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError):
+        return True, ""
+    local = max(1, int(os.environ.get("LOCAL_WORLD_SIZE", "1")))
+    share = avail // local
+    if need * 1.25 <= share:
+        return True, ""
+    return False, (f"e2e needs {need / 1e9:.1f} GB of pinned host memory per rank; "
+                   f"{share / 1e9:.1f} GB available per rank")
 
 
 def run_e2e_zero_copy(args, world: int, dev):
