@@ -57,6 +57,26 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 2-D tiled store of the box at (c0, c1) from shared memory src (bulk-group
+// completion).  c0 * element size must be a multiple of 16 bytes and both
+// coordinates non-negative; the parts of the box outside the tensor are not
+// written.  Every thread that wrote src must have executed
+// fence_proxy_async() before the issuing thread saw those writes.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_addr(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk store of this thread has finished reading
+// its shared-memory source (the buffer may be written again).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until every committed bulk store of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -95,10 +115,13 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // Tensor map of a row-major [rows, cols] bf16 / fp32 matrix with a
-// 32-row x tile_cols box, no swizzle, zero fill outside the matrix.  The row
-// pitch (cols * element size) must be a multiple of 16 bytes.
+// 32-row x tile_cols box, zero fill outside the matrix.  The row pitch
+// (cols * element size) must be a multiple of 16 bytes.  swizzle128: the box
+// rows must be 128 bytes and the shared destination 1024-byte aligned; the
+// 16-byte chunk c of box row r then lands at chunk c ^ (r & 7) of that row.
+// l2_promotion: 0, 128 or 256 (bytes the L2 fetches per request).
 inline cudaError_t encode_tile_map(CUtensorMap* map, const void* x, bool bf16, int64_t rows,
-                                   int64_t cols, int tile_cols) {
+                                   int64_t cols, int tile_cols, bool swizzle128 = false, int l2_promotion = 256) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -107,8 +130,35 @@ inline cudaError_t encode_tile_map(CUtensorMap* map, const void* x, bool bf16, i
   const cuuint32_t estride[2] = {1u, 1u};
   if (encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
              const_cast<void*>(x), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             l2_promotion == 256   ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+             : l2_promotion == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                   : CU_TENSOR_MAP_L2_PROMOTION_NONE,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
+// Tensor map of a row-major [outer, inner] byte matrix (an 8-bit output)
+// for tiled stores of box_inner x box_outer boxes.  inner (the row pitch in
+// bytes) and box_inner must be multiples of 16.  swizzle_bytes 0, 32 or 64:
+// within each box row of box_inner bytes the 16-byte chunk c sits in shared
+// memory at chunk c ^ ((r >> 2) & 1) for 32 (32-byte rows) and
+// c ^ ((r >> 1) & 3) for 64 (64-byte rows); the source must be 1024-byte
+// aligned.
+inline cudaError_t encode_byte_map(CUtensorMap* map, void* q, int64_t outer, int64_t inner, int box_inner,
+                                   int box_outer, int swizzle_bytes) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  const cuuint64_t strides[1] = {(cuuint64_t)inner};
+  const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+  const cuuint32_t estride[2] = {1u, 1u};
+  const CUtensorMapSwizzle sw = swizzle_bytes == 64   ? CU_TENSOR_MAP_SWIZZLE_64B
+                                : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                      : CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q, dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             sw, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   return cudaSuccess;
 }

@@ -90,7 +90,7 @@ def test_mx_dual_full_size(rule):
 def test_mx_dual_edge_values(dtype):
     """Zero / NaN / Inf / subnormal / huge blocks, ragged column tiles,
     both formats, every rule, headroom 0 and 2."""
-    for rows, cols in ((96, 320), (32, 32), (64, 288)):
+    for rows, cols in ((96, 320), (32, 32), (64, 288), (160, 96)):
         x = _edge_tensor(rows, cols, dtype, rows * 7 + cols)
         xb = host_bits(x)
         for fmt in (0, 1):
@@ -140,6 +140,47 @@ def test_cast_transpose_edge_values(dtype, fmt):
     for shape in ((96, 320), (32, 32), (64, 288)):
         _ct_steps(shape, dtype, fmt, 2, 3,
                   lambda t, shape=shape: _edge_tensor(shape[0], shape[1], dtype, 100 * t + shape[1]) * (4.0 ** t))
+
+
+def _at(n, offset):
+    """A device byte buffer of n bytes starting `offset` bytes into a larger
+    allocation (allocations themselves are at least 256-byte aligned)."""
+    return torch.empty(n + 64, dtype=torch.uint8, device="cuda")[offset:offset + n]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_mx_dual_offset_outputs(dtype):
+    """Outputs 16-byte but not 32-byte aligned and E8M0 arrays at odd
+    addresses: same bytes as the oracle."""
+    rows, cols = 160, 288
+    x = _edge_tensor(rows, cols, dtype, 77)
+    xb = host_bits(x)
+    qr = _at(rows * cols, 16).view(rows, cols)
+    er = _at(rows * cols // 32, 1).view(rows, cols // 32)
+    qc = _at(rows * cols, 48).view(cols, rows)
+    ec = _at(rows * cols // 32, 3).view(cols, rows // 32)
+    for fmt in (0, 1):
+        F.mx_cast_dual(x, fmt, 0, 0, qr, er, qc, ec)
+        torch.cuda.synchronize()
+        want = _dual_oracle(xb, fmt, 0, 0)
+        for g, w in zip((qr, er, qc, ec), want[:4]):
+            assert np.array_equal(g.cpu().numpy(), w), fmt
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_cast_transpose_offset_outputs(dtype):
+    rows, cols = 96, 160
+    x = _edge_tensor(rows, cols, dtype, 78)
+    h = F.fp8q_create(0, 0)
+    o = policy.ScalingState(0, 0)
+    q = _at(rows * cols, 16).view(rows, cols)
+    qt = _at(rows * cols, 48).view(cols, rows)
+    F.fp8q_cast_transpose(h, x, q, qt)
+    torch.cuda.synchronize()
+    q_o = o.step(host_bits(x).reshape(-1), NT)[0].reshape(rows, cols)
+    assert np.array_equal(q.cpu().numpy(), q_o)
+    assert np.array_equal(qt.cpu().numpy(), q_o.T)
+    F.fp8q_destroy(h)
 
 
 def test_cast_transpose_argument_checks():
