@@ -13,8 +13,9 @@
 #include <cuda_runtime.h>
 
 #include "fp8q_device.cuh"
-#include "tma.cuh"
 #include "fp8q_internal.cuh"
+#include "tma.cuh"
+#include "warp_tiles.cuh"
 
 namespace fp8q {
 
@@ -123,209 +124,132 @@ cudaError_t launch_mx(const void* x, int dtype, int64_t nelem, int format, int h
 // ---- column-wise blocks ------------------------------------------------------
 //
 // Blocks of 32 consecutive rows of one column (the operand layout a backward
-// matmul reads along its first dimension).  Tiles of 32 rows x TILE_C columns
-// (16 KiB: 256 bf16 or 128 fp32 columns) stream into shared memory through a
-// 4-stage TMA pipeline (cp.async.bulk.tensor.2d, one mbarrier per stage,
-// thread 0 issuing three tiles ahead), so loads stay in flight while the CTA
-// works on the current tile:
-//   1. each thread takes the max over 4 rows of its 16-byte column group;
-//   2. one thread per column combines the 8 partial maxima, computes E,
-//      writes the E8M0 byte (a warp writes 32 consecutive bytes) and
-//      publishes E in shared memory;
-//   3. each thread casts its 4 rows x EPL columns and stores them row-major
-//      (a warp covers one 256-byte (bf16) row segment per store).
-// Every barrier wait is bounded; a tile that does not arrive in time is
-// counted in g_wait_timeouts (fp8q_pipeline_status) and the CTA stops.
+// matmul reads along its first dimension), q and e8m0 row-major like x.
+// Each warp runs the per-warp TMA pipeline of warp_tiles.cuh over 32-row x
+// 128-byte sub-tiles.  Lane l takes bf16 columns 2l, 2l + 1 (one 32-bit
+// shared word per row) or fp32 column l: the block max, E and the cast of
+// its 32 values all stay in the lane.  The lane's bytes go row by row into a
+// swizzled staging tile (a bf16 lane writes one 16-bit pair per row, built
+// with byte permutes) that a TMA tiled store copies to q; the E8M0 bytes of a
+// sub-tile are one coalesced row segment.
 
-constexpr int kColStages = 4;
-constexpr int kColTileBytes = 32 * 32 * 16;            // 32 rows x 32 16-byte groups
+#ifndef FP8Q_COL_STAGES
+#define FP8Q_COL_STAGES 2
+#endif
+#ifndef FP8Q_COL_OBUF
+#define FP8Q_COL_OBUF 2
+#endif
+#ifndef FP8Q_COL_COLF
+#define FP8Q_COL_COLF true
+#endif
+#ifndef FP8Q_COL_L2PROMO
+#define FP8Q_COL_L2PROMO 128
+#endif
+using ColCfg = TpCfg<FP8Q_COL_STAGES, FP8Q_COL_OBUF, 1, FP8Q_COL_COLF, 2048>;
 
 static __device__ unsigned int g_wait_timeouts;
 
+// Byte b of row k of a staging tile with ROWB-byte rows in the swizzled
+// layout of its tensor map (64-byte rows: 16-byte chunk c at c ^ ((k >> 1) & 3);
+// 32-byte rows: c ^ ((k >> 2) & 1)).
+template <int ROWB>
+__device__ __forceinline__ int staged_byte(int k, int b) {
+  const int sw = ROWB == 64 ? ((k >> 1) & 3) : ((k >> 2) & 1);
+  return k * ROWB + ((((b >> 4) ^ sw)) << 4) + (b & 15);
+}
+
 template <int DT, int FMT>
-__global__ void __launch_bounds__(kThreads, 2) mx_colwise_kernel(
-    const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_t cols, uint8_t* __restrict__ q,
-    uint8_t* __restrict__ e8m0, unsigned long long* clipped, int headroom, int rule) {
-  constexpr int EPL = DT == FP8Q_BF16 ? 8 : 4;      // columns per 16-byte group
-  constexpr int GROUPS = 32;                         // 16-byte groups per tile row
-  constexpr int TILE_C = GROUPS * EPL;               // 256 (bf16) / 128 (fp32) columns
+__global__ void __launch_bounds__(kWThreads, 4) mx_colwise_kernel(
+    const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap, int64_t rows,
+    int64_t cols, uint8_t* __restrict__ e8m0, unsigned long long* clipped, int headroom, int rule) {
+  using C = ColCfg;
+  constexpr int TILE_C = TileGeom<DT>::TILE_C;
   extern __shared__ __align__(1024) uint4 dyn_smem[];
-  // kColStages tiles [32][GROUPS], base rounded up to 1024 bytes (TMA needs
-  // at least 128-byte aligned destinations; the launch adds 1 KiB of slack)
-  uint4* const stage_mem = reinterpret_cast<uint4*>(
-      reinterpret_cast<char*>(dyn_smem) + ((1024u - (smem_addr(dyn_smem) & 1023u)) & 1023u));
-  __shared__ __align__(8) uint64_t full[kColStages];
-  __shared__ uint4 part[8][GROUPS];                  // per row-group packed maxima
-  __shared__ __align__(8) signed char s_e[TILE_C];   // E per column, -128 = NaN/Inf block
-  __shared__ __align__(8) unsigned char s_flag[TILE_C];  // 1: block max passes fmax, 2: not finite
-  __shared__ uint32_t red_c[kThreads / 32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t col_tiles = (cols + TILE_C - 1) / TILE_C;
-  const int64_t ntiles = (rows / 32) * col_tiles;
-  const int64_t mine = ntiles > (int64_t)blockIdx.x ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-
-  auto issue = [&](int64_t j) {                      // thread 0: tile j of this CTA
-    const int64_t t = blockIdx.x + j * (int64_t)gridDim.x;
-    const int st = (int)(j % kColStages);
-    mbar_arrive_expect_tx(&full[st], kColTileBytes);
-    tma_load_2d(stage_mem + st * 32 * GROUPS, &tmap, &full[st], (int)((t % col_tiles) * TILE_C),
-                (int)((t / col_tiles) * 32));
-  };
-  if (tid == 0) {
-    for (int i = 0; i < kColStages; ++i) mbar_init(&full[i], 1);
-    fence_barrier_init();
-    prefetch_tensormap(&tmap);
-  }
-  __syncthreads();
-  if (tid == 0)
-    for (int64_t j = 0; j < kColStages - 1 && j < mine; ++j) issue(j);
-
-  uint32_t lclip = 0;
-  for (int64_t j = 0; j < mine; ++j) {
-    // refill the stage every thread finished with in the previous iteration
-    if (tid == 0 && j + kColStages - 1 < mine) {
-      fence_proxy_async();
-      issue(j + kColStages - 1);
-    }
-    const int st = (int)(j % kColStages);
-    const bool ok = mbar_wait(&full[st], (uint32_t)((j / kColStages) & 1));
-    const uint4(*tile)[GROUPS] = reinterpret_cast<const uint4(*)[GROUPS]>(stage_mem + st * 32 * GROUPS);
-    const int64_t t = blockIdx.x + j * (int64_t)gridDim.x;
-    const int64_t r0 = (t / col_tiles) * 32, c0 = (t % col_tiles) * TILE_C;
-
-    // 1. partial maxima: thread (warp w, lane g) covers rows 4w..4w+3 of group g
-    uint32_t pm[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 v = tile[4 * warp + i][lane];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (DT == FP8Q_BF16) pm[k] = vmax_u16x2(pm[k], w[k] & 0x7FFF7FFFu);
-        else pm[k] = max(pm[k], w[k] & 0x7FFFFFFFu);
-      }
-    }
-    part[warp][lane] = make_uint4(pm[0], pm[1], pm[2], pm[3]);
-    if (__syncthreads_or(!ok)) {                     // a tile did not arrive in time
-      if (tid == 0) {
-        atomicAdd(&g_wait_timeouts, 1u);
-        for (int64_t k = j; k < j + kColStages - 1 && k < mine; ++k)   // bounded drain
-          mbar_wait(&full[k % kColStages], (uint32_t)((k / kColStages) & 1));
-      }
+  __shared__ __align__(8) uint64_t full[kWWarps][C::kStages];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t ctiles = (uint32_t)((cols + TILE_C - 1) / TILE_C);
+  uint8_t* region = warp_region<C>(dyn_smem, warp);
+  WarpPipe<C> pipe;
+  pipe.setup(&tmap, reinterpret_cast<uint4*>(region), full[warp], (uint32_t)(rows / 32), ctiles, TILE_C,
+             &g_wait_timeouts);
+  const OutStage<C> out{region + C::kStages * kWTileBytes};
+  pipe.start();
+  uint32_t clip = 0;
+  for (uint32_t j = 0; pipe.valid(pipe.cur); ++j) {
+    if (!pipe.wait(j)) {
+      out.drain();
       return;
     }
-    // 2. one thread per column: final max, exponent, E8M0 byte
-    if (tid < TILE_C) {
-      const int g = tid / EPL, c = tid % EPL;
-      const int word = DT == FP8Q_BF16 ? (c >> 1) : c;
-      uint32_t m = 0;
+    const uint4* tile = pipe.tile(j);
+    const int64_t r0 = pipe.r0(), c0 = pipe.c0();
+    out.acquire();
+    uint8_t* ob = out.buf(j);
+    uint8_t* e8 = e8m0 + (r0 >> 5) * cols;
+    uint32_t w[32];
+    if (DT == FP8Q_BF16) {
+      const int64_t c = c0 + 2 * lane;
+      if (c < cols) {
+        load_column_words(tile, lane, w);
+        const uint32_t pm = tree_absmax32<true>(w);
+        uint32_t o0[8], o1[8];
+        const uint32_t e0 = mx_column<FMT, 0>(w, pm << 16, rule, headroom, clip, o0);
+        const uint32_t e1 = mx_column<FMT, 1>(w, pm & 0xFFFF0000u, rule, headroom, clip, o1);
 #pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        uint32_t v = reinterpret_cast<const uint32_t*>(&part[w][g])[word];
-        if (DT == FP8Q_BF16) v = (c & 1) ? (v & 0xFFFF0000u) : (v << 16);
-        m = max(m, v);
-      }
-      int E;
-      uint32_t byte, flag;
-      if (m >= 0x7F800000u) {                        // NaN / Inf block
-        E = -128;
-        byte = 0xFFu;
-        flag = 2u;
-      } else {
-        E = block_exp<FMT>(m, rule, headroom);
-        byte = (uint32_t)(E + 127);
-        const int be = (int)(fmax_bits(FMT) >> 23) + E;
-        flag = (be < 255 && m > fmax_bits(FMT) + ((uint32_t)E << 23)) ? 1u : 0u;
-      }
-      s_e[tid] = (signed char)E;
-      s_flag[tid] = (unsigned char)flag;
-      if (c0 + tid < cols) e8m0[(r0 / 32) * cols + c0 + tid] = (uint8_t)byte;
-    }
-    __syncthreads();
-    // 3. cast 4 rows x EPL columns, row-major stores.  Columns whose block
-    // max stays within fmax need no per-element check (the common case).
-    const int64_t cbase = c0 + (int64_t)lane * EPL;
-    if (cbase < cols) {
-      signed char eb[EPL];
-      uint32_t any_flag;
-      if (DT == FP8Q_BF16) {
-        *reinterpret_cast<uint2*>(eb) = *reinterpret_cast<const uint2*>(&s_e[lane * EPL]);
-        const uint2 fw = *reinterpret_cast<const uint2*>(&s_flag[lane * EPL]);
-        any_flag = fw.x | fw.y;
-      } else {
-        *reinterpret_cast<uint32_t*>(eb) = *reinterpret_cast<const uint32_t*>(&s_e[lane * EPL]);
-        any_flag = *reinterpret_cast<const uint32_t*>(&s_flag[lane * EPL]);
-      }
-      // a column below its bound cannot clip, so on a flagged tile the clip
-      // test can run on every element; NaN / Inf columns are rare
-      const bool count_clips = (any_flag & 0x01010101u) != 0u;
-      const bool nonfinite = (any_flag & 0x02020202u) != 0u;
-      float sc[EPL];
-#pragma unroll
-      for (int k = 0; k < EPL; ++k)
-        sc[k] = __uint_as_float((uint32_t)(127 - (eb[k] == -128 ? 0 : (int)eb[k])) << 23);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = 4 * warp + i;
-        const uint4 v = tile[r][lane];
-        float f[EPL];
-#pragma unroll
-        for (int k = 0; k < EPL; ++k) f[k] = __uint_as_float(elem_bits<DT>(v, k)) * sc[k];
-        uint32_t ob[2] = {0u, 0u};
-#pragma unroll
-        for (int k = 0; k < EPL; k += 2) ob[k >> 2] |= cvt_pair<FMT>(f[k], f[k + 1]) << ((k & 3) * 8);
-        if (count_clips) {
-#pragma unroll
-          for (int k = 0; k < EPL; ++k) lclip += (eb[k] != -128 && clips<FMT>(f[k])) ? 1u : 0u;
+        for (int m = 0; m < 8; ++m) {               // rows 4m .. 4m + 3: (column 2l, column 2l + 1) pairs
+          const uint32_t lo = __byte_perm(o0[m], o1[m], 0x5140);
+          const uint32_t hi = __byte_perm(o0[m], o1[m], 0x7362);
+          *reinterpret_cast<uint16_t*>(ob + staged_byte<64>(4 * m, 2 * lane)) = (uint16_t)lo;
+          *reinterpret_cast<uint16_t*>(ob + staged_byte<64>(4 * m + 1, 2 * lane)) = (uint16_t)(lo >> 16);
+          *reinterpret_cast<uint16_t*>(ob + staged_byte<64>(4 * m + 2, 2 * lane)) = (uint16_t)hi;
+          *reinterpret_cast<uint16_t*>(ob + staged_byte<64>(4 * m + 3, 2 * lane)) = (uint16_t)(hi >> 16);
         }
-        if (nonfinite) {
-#pragma unroll
-          for (int k = 0; k < EPL; ++k) {
-            if (eb[k] == -128) {                     // NaN / Inf block: sign|0x7F
-              const uint32_t byte = ((elem_bits<DT>(v, k) >> 31) << 7) | 0x7Fu;
-              const int sh = (k & 3) * 8;
-              ob[k >> 2] = (ob[k >> 2] & ~(0xFFu << sh)) | (byte << sh);
-            }
-          }
+        uint8_t* e = e8 + c;
+        if ((reinterpret_cast<uintptr_t>(e) & 1u) == 0) {
+          *reinterpret_cast<uint16_t*>(e) = (uint16_t)(e0 | (e1 << 8));
+        } else {
+          e[0] = (uint8_t)e0;
+          e[1] = (uint8_t)e1;
         }
-        uint8_t* dst = q + (r0 + r) * cols + cbase;
-        if (DT == FP8Q_BF16) __stcs(reinterpret_cast<uint2*>(dst), make_uint2(ob[0], ob[1]));
-        else __stcs(reinterpret_cast<unsigned int*>(dst), ob[0]);
+      }
+    } else {
+      const int64_t c = c0 + lane;
+      if (c < cols) {
+        load_column_words(tile, lane, w);
+        uint32_t o[8];
+        e8[c] = (uint8_t)mx_column<FMT, 2>(w, tree_absmax32<false>(w), rule, headroom, clip, o);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) ob[staged_byte<32>(k, lane)] = (uint8_t)(o[k >> 2] >> (8 * (k & 3)));
       }
     }
-    __syncthreads();                                  // stage / part / s_e reuse
+    out.publish(j, &qmap, nullptr, r0, c0);
+    pipe.release();
   }
-  if (clipped) {
-    lclip = __reduce_add_sync(0xFFFFFFFFu, lclip);
-    if (lane == 0) red_c[warp] = lclip;
-    __syncthreads();
-    if (tid == 0) {
-      unsigned long long tot = 0;
-      for (int i = 0; i < kThreads / 32; ++i) tot += red_c[i];
-      if (tot) atomicAdd(clipped, tot);
-    }
-  }
+  out.drain();
+  clip = __reduce_add_sync(0xFFFFFFFFu, clip);
+  if (clipped && lane == 0 && clip) atomicAdd(clipped, (unsigned long long)clip);
 }
 
 template <int DT, int FMT>
 static cudaError_t launch_mx_col_t(const void* x, int64_t rows, int64_t cols, int headroom, int rule,
                                    uint8_t* q, uint8_t* e8m0, unsigned long long* clipped,
                                    cudaStream_t s, int* launches) {
-  constexpr int EPL = DT == FP8Q_BF16 ? 8 : 4;
-  constexpr int TILE_C = 32 * EPL;
-  constexpr int SMEM = kColStages * kColTileBytes + 1024;
+  using C = ColCfg;
+  constexpr int TILE_C = TileGeom<DT>::TILE_C;
   auto kern = mx_colwise_kernel<DT, FMT>;
+  const int64_t ctiles = (cols + TILE_C - 1) / TILE_C;
+  if ((rows / 32) * ctiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // 32-bit tile counts
   int occ = 1;
-  cudaError_t oe = kernel_occupancy(reinterpret_cast<const void*>(kern), kThreads, SMEM, &occ);
-  if (oe != cudaSuccess) return oe;
-  CUtensorMap map;
-  cudaError_t me = encode_tile_map(&map, x, DT == FP8Q_BF16, rows, cols, TILE_C);
-  if (me != cudaSuccess) return me;
-  const int64_t ntiles = (rows / 32) * ((cols + TILE_C - 1) / TILE_C);
+  cudaError_t e = kernel_occupancy(reinterpret_cast<const void*>(kern), kWThreads, C::kSmemBytes, &occ);
+  if (e != cudaSuccess) return e;
+  CUtensorMap in, qm;
+  e = encode_tile_map(&in, x, DT == FP8Q_BF16, rows, cols, TILE_C, true, FP8Q_COL_L2PROMO);
+  if (e == cudaSuccess) e = encode_byte_map(&qm, q, rows, cols, TILE_C, 32, TILE_C);
+  if (e != cudaSuccess) return e;
+  const long long need = ((rows / 32) * ctiles + kWWarps - 1) / kWWarps;
   long long grid = (long long)sm_count(device_of_current()) * occ;
-  if (grid > ntiles) grid = ntiles;
+  if (grid > need) grid = need;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, kThreads, SMEM, s>>>(map, rows, cols, q, e8m0, clipped, headroom, rule);
+  kern<<<(unsigned)grid, kWThreads, C::kSmemBytes, s>>>(in, qm, rows, cols, e8m0, clipped, headroom, rule);
   ++*launches;
   return cudaGetLastError();
 }
