@@ -325,6 +325,33 @@ def test_mx_ex_edge_values(dtype):
                     assert cl == c_o, (fmt, rule, axis, h)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_mx_colwise_ragged_and_offset(dtype):
+    """Column-wise blocks with cols % 64 == 16 (a last sub-tile holding 16
+    valid columns), a 16-column tensor, q 16-byte but not 32-byte aligned
+    and E8M0 at an odd address."""
+    rng = np.random.default_rng(44)
+    for rows, cols in ((64, 336), (96, 16)):
+        v = rng.standard_normal((rows, cols)) * np.exp(rng.uniform(-20, 20, size=(1, cols)))
+        v[2, cols - 1] = np.nan
+        v[33, 0] = np.inf
+        x = torch.from_numpy(v.astype(np.float32)).to(dtype).cuda()
+        xb = host_bits(x).reshape(rows, cols)
+        qbuf = torch.empty(rows * cols + 64, dtype=torch.uint8, device="cuda")
+        ebuf = torch.empty(rows // 32 * cols + 64, dtype=torch.uint8, device="cuda")
+        q = qbuf[16:16 + rows * cols].view(rows, cols)
+        e8 = ebuf[1:1 + rows // 32 * cols].view(rows // 32, cols)
+        cl = torch.empty(1, dtype=torch.int64, device="cuda")
+        for fmt in (0, 1):
+            for rule in (0, 1):
+                F.mx_cast_ex(x, fmt, rule, 0, 1, q, e8, cl)
+                torch.cuda.synchronize()
+                q_o, e8_o, c_o = coracle.mx_cast_ex(xb, fmt, rule, 0, 1)
+                assert np.array_equal(e8.cpu().numpy(), e8_o), (rows, cols, fmt, rule)
+                assert np.array_equal(q.cpu().numpy(), q_o), (rows, cols, fmt, rule)
+                assert int(cl.item()) == c_o, (rows, cols, fmt, rule)
+
+
 def test_mx_ex_argument_checks():
     x = torch.zeros(48, 64, dtype=torch.bfloat16, device="cuda")
     q = torch.empty(48, 64, dtype=torch.uint8, device="cuda")
