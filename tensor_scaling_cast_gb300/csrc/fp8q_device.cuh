@@ -1,4 +1,5 @@
-// Device helpers of the scaled FP8 cast: conversion, abs-max, exponent rule.
+// Device helpers of the scaled FP8 cast: conversion, abs-max, exponent rule
+// of the per-tensor scale.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -188,32 +189,6 @@ __device__ __forceinline__ int pick_exp(uint32_t a_w, int fmt, int margin, int h
 __device__ __forceinline__ uint32_t no_clip_bound(int fmt, int e) {
   const int be = (int)(fmax_bits(fmt) >> 23) - e;
   return be >= 255 ? 0x7F7FFFFFu : fmax_bits(fmt) - ((uint32_t)e << 23);
-}
-
-// Shared exponent of a block from its amax bits m (finite), per rule:
-//   floor (OCP): E = floor(log2 A) - emax_elem
-//   ceil:        smallest E with A * 2^-E <= fmax; with A = mu * 2^k this is
-//                k - emax_elem + [mu > 1.75]   (fmax = 1.75 * 2^emax_elem)
-//   nearest:     E nearest to log2(A / fmax):   k - emax_elem - [mu < 1.75/sqrt 2],
-//                tested exactly as M^2 < 49 * 2^41 on the 24-bit significand M
-// then + headroom, clamped to [-127, 127]; a zero block gets -127.
-template <int FMT>
-__device__ __forceinline__ int block_exp(uint32_t m, int rule, int headroom) {
-  if (m == 0u) return -127;
-  int k;
-  uint32_t M;
-  if (m >> 23) {
-    k = (int)(m >> 23) - 127;
-    M = 0x800000u | (m & 0x7FFFFFu);
-  } else {
-    const int lb = 31 - __clz((int)m);
-    k = lb - 149;
-    M = m << (23 - lb);
-  }
-  int E = k - emax_elem(FMT);
-  if (rule == FP8Q_MX_CEIL) E += (M > 0xE00000u) ? 1 : 0;
-  else if (rule == FP8Q_MX_NEAREST) E -= ((unsigned long long)M * M < (49ull << 41)) ? 1 : 0;
-  return min(127, max(-127, E + headroom));
 }
 
 }  // namespace fp8q

@@ -14,6 +14,7 @@
 
 #include "fp8q_device.cuh"
 #include "fp8q_internal.cuh"
+#include "mx_device.cuh"
 #include "tma.cuh"
 #include "warp_tiles.cuh"
 

@@ -20,6 +20,7 @@
 
 #include "fp8q_device.cuh"
 #include "fp8q_internal.cuh"
+#include "mx_device.cuh"
 #include "tma.cuh"
 
 namespace fp8q {
