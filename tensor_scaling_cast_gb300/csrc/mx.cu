@@ -150,15 +150,6 @@ using ColCfg = TpCfg<FP8Q_COL_STAGES, FP8Q_COL_OBUF, 1, FP8Q_COL_COLF, 2048>;
 
 static __device__ unsigned int g_wait_timeouts;
 
-// Byte b of row k of a staging tile with ROWB-byte rows in the swizzled
-// layout of its tensor map (64-byte rows: 16-byte chunk c at c ^ ((k >> 1) & 3);
-// 32-byte rows: c ^ ((k >> 2) & 1)).
-template <int ROWB>
-__device__ __forceinline__ int staged_byte(int k, int b) {
-  const int sw = ROWB == 64 ? ((k >> 1) & 3) : ((k >> 2) & 1);
-  return k * ROWB + ((((b >> 4) ^ sw)) << 4) + (b & 15);
-}
-
 template <int DT, int FMT>
 __global__ void __launch_bounds__(kWThreads, 4) mx_colwise_kernel(
     const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap, int64_t rows,

@@ -16,9 +16,11 @@
 // per 32-row x 128-byte sub-tile:
 //   A. row pass: row l, i.e. 2 (bf16) / 1 (fp32) 32-element row blocks, read
 //      as 16-byte chunks, its 32 output bytes per block staged row-major;
-//   B. column pass: bf16 columns 2l and 2l + 1 (one 32-bit word per row) or
-//      fp32 column l, its 32 output bytes per column staged as one row of the
-//      transposed part.
+//   B. column pass: bf16 columns 2l and 2l + 1 or fp32 column l, its 32
+//      output bytes per column staged as one row of the transposed part.
+//      The MX dual reads the column from the input tile (one 32-bit word per
+//      row) and casts it with the column block's own scale; the per-tensor
+//      cast reads back the bytes the row pass staged (same scale, same bytes).
 // Both parts leave through TMA tiled stores.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -266,28 +268,36 @@ __global__ void __launch_bounds__(kWThreads, FP8Q_TP_MINB) cast_transpose_kernel
       pack_row<DT, NG>(t, o);
       stage32<QROWB>(ob, lane, b, o);
     }
-    // B. transposed (a NaN anywhere in the sub-tile sends the columns through
-    // the sign-keeping fix)
     lmax = max(lmax, tmax);
-    const bool has_nan = __any_sync(0xFFFFFFFFu, tmax > 0x7F800000u);
-    uint32_t w[32], o[8];
+    pipe.release();                                  // the input stage is no longer read
+    // B. transposed: q^T holds q's bytes, read back column-wise from the
+    // row-major part and assembled with byte permutes
+    __syncwarp();                                    // the row-major part is in place
     if (DT == FP8Q_BF16) {
-      if (c0 + 2 * lane < cols) {
-        load_column_words(tile, lane, w);
-        ct_column<FMT, 0>(w, has_nan, s, o);
-        stage32<32>(ob + 2048, 2 * lane, 0, o);
-        ct_column<FMT, 1>(w, has_nan, s, o);
-        stage32<32>(ob + 2048, 2 * lane + 1, 0, o);
+      uint32_t a[8], bb[8];                          // columns 2l and 2l + 1, 4 rows per word
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        uint32_t u[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) u[i] = *reinterpret_cast<const uint16_t*>(ob + staged_byte<64>(4 * m + i, 2 * lane));
+        const uint32_t p01 = __byte_perm(u[0], u[1], 0x5410), p23 = __byte_perm(u[2], u[3], 0x5410);
+        a[m] = __byte_perm(p01, p23, 0x6420);
+        bb[m] = __byte_perm(p01, p23, 0x7531);
       }
+      stage32<32>(ob + 2048, 2 * lane, 0, a);
+      stage32<32>(ob + 2048, 2 * lane + 1, 0, bb);
     } else {
-      if (c0 + lane < cols) {
-        load_column_words(tile, lane, w);
-        ct_column<FMT, 2>(w, has_nan, s, o);
-        stage32<32>(ob + 2048, lane, 0, o);
+      uint32_t a[8];                                 // column l, 4 rows per word
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        uint32_t u[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) u[i] = ob[staged_byte<32>(4 * m + i, lane)];
+        a[m] = __byte_perm(__byte_perm(u[0], u[1], 0x0040), __byte_perm(u[2], u[3], 0x0040), 0x5410);
       }
+      stage32<32>(ob + 2048, lane, 0, a);
     }
     out.publish(j, &qmap, &qtmap, r0, c0);
-    pipe.release();
   }
   out.drain();
   // per-warp totals, then the ticket: the warp completing the tensor finishes it

@@ -145,6 +145,15 @@ __device__ __forceinline__ void stage32(uint8_t* buf, int r, int half, const uin
   stage16<ROWB>(buf, r, 2 * half + 1, o[4], o[5], o[6], o[7]);
 }
 
+// Byte b of row k of a staging tile with ROWB-byte rows in the swizzled
+// layout of its tensor map (64-byte rows: 16-byte chunk c at c ^ ((k >> 1) & 3);
+// 32-byte rows: c ^ ((k >> 2) & 1)).
+template <int ROWB>
+__device__ __forceinline__ int staged_byte(int k, int b) {
+  const int sw = ROWB == 64 ? ((k >> 1) & 3) : ((k >> 2) & 1);
+  return k * ROWB + ((((b >> 4) ^ sw)) << 4) + (b & 15);
+}
+
 // One MX column block (column HI of the lane's words): its 32 bytes into o,
 // returns its E8M0 byte.  m = the block's max |x| bits.
 template <int FMT, int HI>
@@ -183,27 +192,14 @@ __device__ __forceinline__ void store_e8_run(uint8_t* e8, E8Acc<CH> acc, uint32_
   for (uint32_t k = 0; k < n; ++k) e8[k] = (uint8_t)(acc >> (8 * k));
 }
 
-// One per-tensor column (column HI of the lane's words) with scale s.
-// has_nan: the sub-tile holds a NaN somewhere (its sign must be kept).
-template <int FMT, int HI>
-__device__ __forceinline__ void ct_column(const uint32_t (&w)[32], bool has_nan, float s, uint32_t (&o)[8]) {
-  cast32<FMT, HI>(w, s, o);
-  if (has_nan) {
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const uint32_t b = half_bits<HI>(w[k]);
-      if ((b & 0x7FFFFFFFu) > 0x7F800000u) set_byte(o, k, ((b >> 31) << 7) | 0x7Fu);
-    }
-  }
-}
-
 // Work order.  The sub-tiles form a grid of rtiles x ctiles (32 rows x
 // tile_c columns each).  A chunk is CH consecutive row tiles of one
 // column tile (fewer at the bottom edge); chunks are numbered row-chunk
-// fastest and dealt to the warps round-robin (warp w takes chunks w,
-// w + nwarps, ...).  Within a chunk a warp walks down the rows, so it can
-// collect each column's CH transposed-scale bytes into one store.  The
-// warps in flight together cover a band of adjacent column strips.
+// fastest (COLF false: the warps in flight together cover a band of
+// adjacent column strips) or column-tile fastest (COLF true: a band of
+// adjacent row chunks), and dealt to the warps round-robin (warp w takes
+// chunks w, w + nwarps, ...).  Within a chunk a warp walks down the rows, so
+// it can collect each column's CH transposed-scale bytes into one store.
 template <int CH, bool COLF>
 struct TileCursor {
   uint32_t v;                    // chunk
