@@ -43,6 +43,8 @@ def parse():
     p.add_argument("--workload", default="decoder",
                    choices=["decoder", "current", "spike", "grad", "mx", "transpose", "single"])
     p.add_argument("--n", type=int, default=1 << 26, help="elements for --workload single")
+    p.add_argument("--single-dtype", default="bf16", choices=["bf16", "fp32"],
+                   help="input type for --workload single")
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
@@ -123,7 +125,7 @@ class Part:
 
 
 class Workload:
-    def __init__(self, kind: str, n: int, device, host_io: bool = False):
+    def __init__(self, kind: str, n: int, device, host_io: bool = False, single_dtype: str = "bf16"):
         """host_io: inputs and outputs live in pinned host memory and the
         kernels read / write them directly over NVLink-C2C (zero-copy)."""
         import torch
@@ -243,9 +245,11 @@ class Workload:
         else:
             g = torch.Generator(device=dev)
             g.manual_seed(1)
-            x = torch.randn(n, generator=g, device=dev).to(torch.bfloat16)
+            x = torch.randn(n, generator=g, device=dev)
+            if single_dtype == "bf16":
+                x = x.to(torch.bfloat16)
             grouped("cast", [x], [F.E4M3], 16)
-            self.name = f"single bf16 tensor of {n} elements, E4M3, max-window 16"
+            self.name = f"single {single_dtype} tensor of {n} elements, E4M3, max-window 16"
         self.step_bytes = sum(p.bytes for p in self.parts)
         # small launches cannot be fed from Python fast enough: those
         # workloads are timed by replaying a CUDA graph of `graph_steps` steps
@@ -433,7 +437,7 @@ def run_ours(args, rank: int, world: int):
     if world > 1:
         dist.barrier()
     F.load()
-    W = Workload(args.workload, args.n, dev)
+    W = Workload(args.workload, args.n, dev, single_dtype=args.single_dtype)
     torch.cuda.synchronize()
     clocks = Clocks(local)
     clocks.start()
@@ -708,7 +712,7 @@ def run_e2e_zero_copy(args, world: int, dev):
     straight to the C ABI: the kernels read the inputs and write the
     results over NVLink-C2C, so each step moves the same host bytes."""
     import torch
-    W = Workload(args.workload, args.n, dev, host_io=True)
+    W = Workload(args.workload, args.n, dev, host_io=True, single_dtype=args.single_dtype)
     for k in range(3):
         W.step(k)
     torch.cuda.synchronize()
