@@ -19,6 +19,15 @@
 // all tensors of the group form one index space cut into gridDim.x equal
 // contiguous ranges, one per CTA.  A CTA therefore visits few tensors and
 // flushes its partial results once per tensor.
+//
+// Launch: programmatic dependent launch.  Each CTA first waits until the
+// preceding grid in the stream has completed and its writes are visible
+// (griddepcontrol.wait), before any global access, then lets the next grid
+// start launching (griddepcontrol.launch_dependents).  The next launch's
+// set-up thus overlaps this grid's tail, and every dependency stays ordered
+// (a cast reads the state the previous cast on the same handle left).  The
+// grid is one wave (SMs x resident CTAs), so a dependent grid only takes SM
+// slots that this one's finished CTAs free.
 #include <cuda_runtime.h>
 
 #include "fp8q_device.cuh"
@@ -26,6 +35,9 @@
 #include "state.cuh"
 
 namespace fp8q {
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <int DT>
 struct Tr {
@@ -199,6 +211,8 @@ __global__ void __launch_bounds__(kThreads, UF ? 3 : 4) cast_group_kernel(const 
   __shared__ uint32_t s_nonfin;                   // non-finite inputs of the current segment
   __shared__ uint32_t red_m[kThreads / 32], red_c[kThreads / 32], red_u[kThreads / 32];
   if (threadIdx.x == 0) s_nonfin = 0u;            // published by the first __syncthreads below
+  pdl_wait();
+  pdl_launch_dependents();
   const int total = p.h.total_chunks;
   int c = (int)(((long long)blockIdx.x * total) / gridDim.x);
   const int c_end = (int)(((long long)(blockIdx.x + 1) * total) / gridDim.x);
@@ -232,14 +246,20 @@ __global__ void __launch_bounds__(kThreads, UF ? 3 : 4) cast_group_kernel(const 
       DevState* st = d.st;
       const uint32_t lnonfin = s_nonfin;   // all slow-path adds happened before the reduction's barrier
       s_nonfin = 0u;
-      if (lmax) atomicMax(&st->amax_acc, lmax);
-      if (lclip) atomicAdd(&st->clip_acc, (unsigned long long)lclip);
-      if (lnonfin) atomicAdd(&st->nonfinite_acc, (unsigned long long)lnonfin);
-      if (UF && lunder) atomicAdd(&st->underflow_acc, (unsigned long long)lunder);
-      __threadfence();
-      const unsigned done = (unsigned)(seg_end - c);
-      const unsigned prev = atomicAdd(&st->ticket, done);
-      if (prev + done == (unsigned)(t_end - t_begin)) finish_tensor(st, p.h, t, e);
+      if (c == t_begin && seg_end == t_end) {
+        // this CTA holds the whole tensor: its totals are final, no
+        // accumulator or ticket round trip
+        publish_and_advance(st, p.h, t, e, lmax, lclip, lnonfin, UF ? lunder : 0u);
+      } else {
+        if (lmax) atomicMax(&st->amax_acc, lmax);
+        if (lclip) atomicAdd(&st->clip_acc, (unsigned long long)lclip);
+        if (lnonfin) atomicAdd(&st->nonfinite_acc, (unsigned long long)lnonfin);
+        if (UF && lunder) atomicAdd(&st->underflow_acc, (unsigned long long)lunder);
+        __threadfence();
+        const unsigned done = (unsigned)(seg_end - c);
+        const unsigned prev = atomicAdd(&st->ticket, done);
+        if (prev + done == (unsigned)(t_end - t_begin)) finish_tensor(st, p.h, t, e);
+      }
     }
     __syncthreads();
     c = seg_end;
@@ -250,6 +270,8 @@ __global__ void __launch_bounds__(kThreads, UF ? 3 : 4) cast_group_kernel(const 
 template <int MAXT>
 __global__ void __launch_bounds__(kThreads, 4) amax_group_kernel(const __grid_constant__ GroupParams<MAXT> p) {
   __shared__ uint32_t red_m[kThreads / 32], red_c[kThreads / 32];
+  pdl_wait();
+  pdl_launch_dependents();
   const int total = p.h.total_chunks;
   int c = (int)(((long long)blockIdx.x * total) / gridDim.x);
   const int c_end = (int)(((long long)(blockIdx.x + 1) * total) / gridDim.x);
@@ -289,9 +311,19 @@ static cudaError_t launch_group_t(const GroupHeader& h, const TensorDesc* d, int
   long long grid = (long long)sm_count(dev) * occ;
   if (grid > h.total_chunks) grid = h.total_chunks;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, kThreads, 0, s>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
   ++*launches;
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int KIND>

@@ -46,13 +46,12 @@ static __device__ __forceinline__ void warp_exp(const DevState* st, int mode, in
   if (threadIdx.x == 0) *s_e = state_exp(st, a_w);
 }
 
-// Thread 0 of the CTA that completes the tensor: publish and advance state.
-static __device__ void finish_tensor(DevState* st, const GroupHeader& h, int t, int e) {
-  __threadfence();
-  uint32_t a = atomicAdd(&st->amax_acc, 0u);
-  const unsigned long long cl = atomicAdd(&st->clip_acc, 0ull);
-  const unsigned long long nf = atomicAdd(&st->nonfinite_acc, 0ull);
-  const unsigned long long uf = atomicAdd(&st->underflow_acc, 0ull);
+// Publish one cast's results (amax a, clipped, non-finite and underflow
+// counts, exponent e) and advance the handle's state.  Thread 0 of the CTA
+// that completes the tensor.
+static __device__ void publish_and_advance(DevState* st, const GroupHeader& h, int t, int e, uint32_t a,
+                                           unsigned long long cl, unsigned long long nf,
+                                           unsigned long long uf) {
   if (a > 0x7F800000u) a = 0x7FC00000u;        // canonical NaN
   const int idx = h.out_offset + t;
   if (h.amax) h.amax[idx] = __uint_as_float(a);
@@ -83,6 +82,17 @@ static __device__ void finish_tensor(DevState* st, const GroupHeader& h, int t, 
   st->underflow_acc = 0ull;
   st->pre_amax = 0u;
   st->ticket = 0u;
+}
+
+// Thread 0 of the CTA whose ticket completes the tensor: the totals are the
+// accumulators every CTA of the tensor added into.
+static __device__ void finish_tensor(DevState* st, const GroupHeader& h, int t, int e) {
+  __threadfence();
+  const uint32_t a = atomicAdd(&st->amax_acc, 0u);
+  const unsigned long long cl = atomicAdd(&st->clip_acc, 0ull);
+  const unsigned long long nf = atomicAdd(&st->nonfinite_acc, 0ull);
+  const unsigned long long uf = atomicAdd(&st->underflow_acc, 0ull);
+  publish_and_advance(st, h, t, e, a, cl, nf, uf);
 }
 
 }  // namespace fp8q
