@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kThreads, 4) mx_kernel(const char* __restrict_
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t e0 = base + (int64_t)(u * kThreads + threadIdx.x) * EPL;
-      uint32_t m = unpack_max<DT>(absmax_load<DT>(r[u]));
+      uint32_t m = mag_bits<DT>(mag_load<DT>(r[u]));
 #pragma unroll
       for (int o = 1; o < LPB; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
       uint2 out;

@@ -9,6 +9,35 @@
 
 namespace fp8q {
 
+// Larger magnitude in one instruction: max(|a|, |b|) per bf16 lane of a
+// packed pair (or of two fp32 values), the exact larger magnitude with its
+// sign bit set to the XOR of the input signs, and the canonical NaN when
+// either input is NaN.  The caller masks the sign bits once at the end, which
+// leaves the same bits as an integer max of the masked abs bits (NaN above
+// Inf above every finite value).
+template <int DT>
+__device__ __forceinline__ uint32_t mag_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  if (DT == FP8Q_BF16) {
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  } else {
+    float f;
+    asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(f) : "f"(__uint_as_float(a)), "f"(__uint_as_float(b)));
+    r = __float_as_uint(f);
+  }
+  return r;
+}
+// Over one 16-byte load (packed pairs for bf16; signs not yet masked).
+template <int DT>
+__device__ __forceinline__ uint32_t mag_load(const uint4& v) {
+  return mag_max<DT>(mag_max<DT>(v.x, v.y), mag_max<DT>(v.z, v.w));
+}
+// Masked magnitude as fp32 bits (for bf16: the larger of the two lanes).
+template <int DT>
+__device__ __forceinline__ uint32_t mag_bits(uint32_t m) {
+  return unpack_max<DT>(m & (DT == FP8Q_BF16 ? 0x7FFF7FFFu : 0x7FFFFFFFu));
+}
+
 // Shared exponent of a block from its amax bits m (finite), per rule:
 //   floor (OCP): E = floor(log2 A) - emax_elem
 //   ceil:        smallest E with A * 2^-E <= fmax; with A = mu * 2^k this is

@@ -119,10 +119,10 @@ __global__ void __launch_bounds__(kWThreads, FP8Q_TP_MINB) mx_dual_kernel(
     for (int b = 0; b < G::BPR; ++b) {
       uint4 v[NG];
       load_row_block<NG>(tile, lane, b, v);
-      uint32_t pm = absmax_load<DT>(v[0]);
+      uint32_t pm = mag_load<DT>(v[0]);
 #pragma unroll
-      for (int k = 1; k < NG; ++k) pm = absmax_merge<DT>(pm, absmax_load<DT>(v[k]));
-      const uint32_t m = unpack_max<DT>(pm);
+      for (int k = 1; k < NG; ++k) pm = mag_max<DT>(pm, mag_load<DT>(v[k]));
+      const uint32_t m = mag_bits<DT>(pm);
       uint32_t o[8];
       uint32_t ebyte;
       if (m >= 0x7F800000u) {                        // NaN / Inf block
@@ -252,10 +252,10 @@ __global__ void __launch_bounds__(kWThreads, FP8Q_TP_MINB) cast_transpose_kernel
     for (int b = 0; b < G::BPR; ++b) {
       uint4 v[NG];
       load_row_block<NG>(tile, lane, b, v);
-      uint32_t pm = absmax_load<DT>(v[0]);
+      uint32_t pm = mag_load<DT>(v[0]);
 #pragma unroll
-      for (int k = 1; k < NG; ++k) pm = absmax_merge<DT>(pm, absmax_load<DT>(v[k]));
-      const uint32_t m = unpack_max<DT>(pm);
+      for (int k = 1; k < NG; ++k) pm = mag_max<DT>(pm, mag_load<DT>(v[k]));
+      const uint32_t m = mag_bits<DT>(pm);
       tmax = max(tmax, m);
       uint2 t[NG];
 #pragma unroll

@@ -66,21 +66,21 @@ __device__ __forceinline__ void pack_row(const uint2 (&t)[NG], uint32_t (&o)[8])
   }
 }
 
-// Max of |.| over 32 words as a depth-5 tree (a serial chain would leave
-// each thread waiting on 32 dependent max operations).  Packed bf16 pairs
-// (PAIRS) or fp32 bit patterns.
+// Max of |.| over 32 words as a depth-5 tree of one-instruction magnitude
+// maxima (a serial chain would leave each thread waiting on 32 dependent
+// operations).  Packed bf16 pairs (PAIRS, both lanes masked) or fp32 bit
+// patterns.
 template <bool PAIRS>
 __device__ __forceinline__ uint32_t tree_absmax32(const uint32_t (&w)[32]) {
-  const uint32_t mask = PAIRS ? 0x7FFF7FFFu : 0x7FFFFFFFu;
+  constexpr int DT = PAIRS ? FP8Q_BF16 : FP8Q_F32;
   uint32_t t[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i)
-    t[i] = PAIRS ? vmax_u16x2(w[2 * i] & mask, w[2 * i + 1] & mask) : max(w[2 * i] & mask, w[2 * i + 1] & mask);
+  for (int i = 0; i < 16; ++i) t[i] = mag_max<DT>(w[2 * i], w[2 * i + 1]);
 #pragma unroll
   for (int n = 8; n >= 1; n >>= 1)
 #pragma unroll
-    for (int i = 0; i < n; ++i) t[i] = PAIRS ? vmax_u16x2(t[2 * i], t[2 * i + 1]) : max(t[2 * i], t[2 * i + 1]);
-  return t[0];
+    for (int i = 0; i < n; ++i) t[i] = mag_max<DT>(t[2 * i], t[2 * i + 1]);
+  return t[0] & (PAIRS ? 0x7FFF7FFFu : 0x7FFFFFFFu);
 }
 
 // Word l of each of the 32 rows of a swizzled sub-tile: a bf16 column pair
