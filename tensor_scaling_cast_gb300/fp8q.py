@@ -99,8 +99,10 @@ def _check(status: int, what: str):
         raise Fp8qError(status, what, detail)
 
 
+# The entry points declare their pointer arguments as c_void_p, so plain
+# Python ints (and None for NULL) are passed straight through.
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _dtype(t: torch.Tensor) -> int:
@@ -111,10 +113,17 @@ def _dtype(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported input dtype {t.dtype}: bf16 or fp32")
 
 
+# torch's raw getter of the current stream (the public path builds a Stream
+# object per call); falls back to the public path where it is absent.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream):
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def fp8q_pipeline_status() -> int:
@@ -152,19 +161,19 @@ def fp8q_create_ex(fmt: int, window: int, margin: int = 0, hysteresis: int = 0,
 def fp8q_get_estimator_state(h: int):
     """(running average or None, number of casts)."""
     a, ha, st = ctypes.c_float(), ctypes.c_int(), ctypes.c_longlong()
-    _check(load().fp8q_get_estimator_state(ctypes.c_void_p(h), ctypes.byref(a), ctypes.byref(ha),
+    _check(load().fp8q_get_estimator_state(h, ctypes.byref(a), ctypes.byref(ha),
                                            ctypes.byref(st)), "fp8q_get_estimator_state")
     return (a.value if ha.value else None), st.value
 
 
 def fp8q_set_estimator_state(h: int, average, steps: int):
-    _check(load().fp8q_set_estimator_state(ctypes.c_void_p(h), 0.0 if average is None else average,
+    _check(load().fp8q_set_estimator_state(h, 0.0 if average is None else average,
                                            0 if average is None else 1, steps),
            "fp8q_set_estimator_state")
 
 
 def fp8q_destroy(h: int):
-    _check(load().fp8q_destroy(ctypes.c_void_p(h)), "fp8q_destroy")
+    _check(load().fp8q_destroy(h), "fp8q_destroy")
 
 
 def fp8q_cast(h: int, x: torch.Tensor, q: torch.Tensor, scale_inv=None, amax=None, clipped=None,
@@ -172,7 +181,7 @@ def fp8q_cast(h: int, x: torch.Tensor, q: torch.Tensor, scale_inv=None, amax=Non
     """x: contiguous bf16/fp32 CUDA tensor; q: uint8 CUDA tensor of x.numel()
     bytes; scale_inv / amax: float32 CUDA scalars; clipped: int64 CUDA scalar
     (read as uint64)."""
-    _check(load().fp8q_cast(ctypes.c_void_p(h), _ptr(x), _dtype(x), x.numel(), _ptr(q),
+    _check(load().fp8q_cast(h, _ptr(x), _dtype(x), x.numel(), _ptr(q),
                             _ptr(scale_inv), _ptr(amax), _ptr(clipped), _stream(stream)),
            "fp8q_cast")
 
@@ -214,13 +223,13 @@ def fp8q_loss_scaler_create(init_scale: float, growth_interval: int, min_scale: 
 
 
 def fp8q_loss_scaler_destroy(h: int):
-    _check(load().fp8q_loss_scaler_destroy(ctypes.c_void_p(h)), "fp8q_loss_scaler_destroy")
+    _check(load().fp8q_loss_scaler_destroy(h), "fp8q_loss_scaler_destroy")
 
 
 def fp8q_loss_scaler_update(h: int, nonfinite: torch.Tensor, scale=None, skip=None, stream=None):
     """nonfinite: int64 CUDA tensor of counts; scale: float32 CUDA scalar;
     skip: int32 CUDA scalar."""
-    _check(load().fp8q_loss_scaler_update(ctypes.c_void_p(h), _ptr(nonfinite), nonfinite.numel(),
+    _check(load().fp8q_loss_scaler_update(h, _ptr(nonfinite), nonfinite.numel(),
                                           _ptr(scale), _ptr(skip), _stream(stream)),
            "fp8q_loss_scaler_update")
 
@@ -228,7 +237,7 @@ def fp8q_loss_scaler_update(h: int, nonfinite: torch.Tensor, scale=None, skip=No
 def fp8q_loss_scaler_read(h: int):
     """(scale, clean-step streak)."""
     sc, g = ctypes.c_float(), ctypes.c_int()
-    _check(load().fp8q_loss_scaler_read(ctypes.c_void_p(h), ctypes.byref(sc), ctypes.byref(g)),
+    _check(load().fp8q_loss_scaler_read(h, ctypes.byref(sc), ctypes.byref(g)),
            "fp8q_loss_scaler_read")
     return sc.value, g.value
 
@@ -263,7 +272,7 @@ def fp8q_cast_transpose(h: int, x: torch.Tensor, q, qt, scale_inv=None, amax=Non
                         stream=None):
     """Per-tensor cast of x [rows, cols] to q [rows, cols] and qt [cols, rows]."""
     rows, cols = x.shape
-    _check(load().fp8q_cast_transpose(ctypes.c_void_p(h), _ptr(x), _dtype(x), rows, cols, _ptr(q),
+    _check(load().fp8q_cast_transpose(h, _ptr(x), _dtype(x), rows, cols, _ptr(q),
                                       _ptr(qt), _ptr(scale_inv), _ptr(amax), _ptr(clipped),
                                       _stream(stream)), "fp8q_cast_transpose")
 
@@ -271,7 +280,7 @@ def fp8q_cast_transpose(h: int, x: torch.Tensor, q, qt, scale_inv=None, amax=Non
 def fp8q_amax_history(h: int, capacity: int = MAX_WINDOW) -> list[float]:
     buf = (ctypes.c_float * max(1, capacity))()
     nv = ctypes.c_int()
-    _check(load().fp8q_amax_history(ctypes.c_void_p(h), buf, capacity, ctypes.byref(nv)),
+    _check(load().fp8q_amax_history(h, buf, capacity, ctypes.byref(nv)),
            "fp8q_amax_history")
     return [buf[i] for i in range(nv.value)]
 
@@ -280,20 +289,20 @@ def fp8q_scale_state(h: int):
     """(previous exponent or None, number of casts)."""
     e = ctypes.c_int()
     st = ctypes.c_longlong()
-    _check(load().fp8q_scale_state(ctypes.c_void_p(h), ctypes.byref(e), ctypes.byref(st)),
+    _check(load().fp8q_scale_state(h, ctypes.byref(e), ctypes.byref(st)),
            "fp8q_scale_state")
     return (None if e.value == NO_EXP else e.value), st.value
 
 
 def fp8q_set_history(h: int, values, prev_exp=None):
     buf = (ctypes.c_float * max(1, len(values)))(*values)
-    _check(load().fp8q_set_history(ctypes.c_void_p(h), buf, len(values),
+    _check(load().fp8q_set_history(h, buf, len(values),
                                    NO_EXP if prev_exp is None else int(prev_exp)),
            "fp8q_set_history")
 
 
 def fp8q_reset(h: int):
-    _check(load().fp8q_reset(ctypes.c_void_p(h)), "fp8q_reset")
+    _check(load().fp8q_reset(h), "fp8q_reset")
 
 
 def fp8q_error_stats(x: torch.Tensor, q: torch.Tensor, fmt: int, scale_inv: torch.Tensor,
@@ -334,10 +343,11 @@ class ScaledCast:
         dev = x.device
         if q is None:
             q = torch.empty(x.shape, dtype=torch.uint8, device=dev)
-        outs = torch.empty(2, dtype=torch.float32, device=dev)
-        clipped = torch.empty(1, dtype=torch.int64, device=dev)
-        fp8q_cast(self.handle, x, q, outs[0:1], outs[1:2], clipped, stream)
-        return q, outs[0:1], outs[1:2], clipped
+        # one 16-byte allocation: scale_inv f32, amax f32, clipped i64
+        outs = torch.empty(4, dtype=torch.float32, device=dev)
+        scale_inv, amax, clipped = outs[0:1], outs[1:2], outs[2:4].view(torch.int64)
+        fp8q_cast(self.handle, x, q, scale_inv, amax, clipped, stream)
+        return q, scale_inv, amax, clipped
 
     def history(self):
         return fp8q_amax_history(self.handle, max(1, self.window))
