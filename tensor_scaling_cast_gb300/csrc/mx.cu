@@ -20,6 +20,10 @@
 
 namespace fp8q {
 
+// Lane-loads per thread per tile of the row-wise kernel: 4 (16 KiB tiles)
+// measured 2-3% faster than the grouped cast's 8 on bf16 [16384, 8192].
+constexpr int kMxUnroll = 4;
+
 template <int DT, int FMT>
 __global__ void __launch_bounds__(kThreads, 4) mx_kernel(const char* __restrict__ x, int64_t nelem,
                                                       uint8_t* __restrict__ q,
@@ -29,22 +33,22 @@ __global__ void __launch_bounds__(kThreads, 4) mx_kernel(const char* __restrict_
   constexpr int EPL = DT == FP8Q_BF16 ? 8 : 4;    // elements per lane-load
   constexpr int ESZ = DT == FP8Q_BF16 ? 2 : 4;
   constexpr int LPB = 32 / EPL;                   // lanes per 32-element block
-  constexpr int64_t TILE = (int64_t)kThreads * kUnroll * EPL;
+  constexpr int64_t TILE = (int64_t)kThreads * kMxUnroll * EPL;
   __shared__ uint32_t red_c[kThreads / 32];
   const int lane = threadIdx.x & 31;
   uint32_t lclip = 0;
   const int64_t ntiles = (nelem + TILE - 1) / TILE;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const int64_t base = tile * TILE;
-    uint4 r[kUnroll];
+    uint4 r[kMxUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < kMxUnroll; ++u) {
       const int64_t e0 = base + (int64_t)(u * kThreads + threadIdx.x) * EPL;
       // nelem is a multiple of 32, so a lane-load is entirely in or out
       r[u] = e0 < nelem ? __ldcs(reinterpret_cast<const uint4*>(x + e0 * ESZ)) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < kMxUnroll; ++u) {
       const int64_t e0 = base + (int64_t)(u * kThreads + threadIdx.x) * EPL;
       uint32_t m = mag_bits<DT>(mag_load<DT>(r[u]));
 #pragma unroll
@@ -96,7 +100,7 @@ static cudaError_t launch_mx_t(const void* x, int64_t nelem, int headroom, int r
                                uint8_t* e8m0, unsigned long long* clipped, cudaStream_t s,
                                int* launches) {
   constexpr int EPL = DT == FP8Q_BF16 ? 8 : 4;
-  constexpr int64_t TILE = (int64_t)kThreads * kUnroll * EPL;
+  constexpr int64_t TILE = (int64_t)kThreads * kMxUnroll * EPL;
   int occ = 1;
   cudaError_t oe = kernel_occupancy(reinterpret_cast<const void*>(mx_kernel<DT, FMT>), kThreads, 0, &occ);
   if (oe != cudaSuccess) return oe;

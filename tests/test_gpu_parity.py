@@ -366,7 +366,7 @@ def test_mx_ex_argument_checks():
 # edge cases of the per-tensor path
 # ---------------------------------------------------------------------------
 
-SIZES = [0, 1, 15, 16, 17, 31, 33, 4095, 8191, 8192, 8193, 16383, 16384, 16385, 65537,
+SIZES = [0, 1, 15, 16, 17, 31, 33, 4095, 4096, 4097, 8191, 8192, 8193, 16383, 16384, 16385, 65537,
          (1 << 20) + 3]
 
 
