@@ -75,8 +75,8 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = ["tensor_scaling_cast_gb300/csrc/cast.cu", "tensor_scaling_cast_gb300/csrc/fp8q_device.cuh",
-                  "tensor_scaling_cast_gb300/csrc/fp8q_internal.cuh"]
+KERNEL_SOURCES = ["tensor_scaling_cast_gb300/csrc/cast_kernels.cuh", "tensor_scaling_cast_gb300/csrc/state.cuh",
+                  "tensor_scaling_cast_gb300/csrc/fp8q_device.cuh", "tensor_scaling_cast_gb300/csrc/fp8q_internal.cuh"]
 TRAFFIC_FILE = "profiles/traffic_cast_group_kernel_decoder_1b1.md"
 
 
