@@ -209,3 +209,42 @@ def test_pipeline_wait_gives_up_and_is_reported():
     got = _dual_gpu(x, 0, 0, 0)
     want = _dual_oracle(host_bits(x), 0, 0, 0)
     assert all(np.array_equal(g, w) for g, w in zip(got[:4], want[:4]))
+
+
+def test_random_shapes_all_tiled_paths():
+    """Randomly drawn shapes (ragged 64-column sub-tiles, partial row chunks,
+    tails of 16 columns), both input types, both formats, every MX rule:
+    column-wise MX, the MX dual and the per-tensor cast + transpose, byte for
+    byte against the oracle."""
+    rng = np.random.default_rng(2024)
+    for trial in range(24):
+        dtype = (torch.bfloat16, torch.float32)[trial % 2]
+        fmt = (trial // 2) % 2
+        rule = (trial // 4) % 3
+        rows = 32 * int(rng.integers(1, 18))
+        cols32 = 32 * int(rng.integers(1, 20))
+        x = _edge_tensor(rows, cols32, dtype, 500 + trial) if trial % 3 == 0 else \
+            torch.from_numpy((rng.standard_normal((rows, cols32)) *
+                              np.exp(rng.uniform(-8, 8, size=(1, cols32)))).astype(np.float32)).to(dtype).cuda()
+        xb = host_bits(x)
+        # MX dual
+        got = _dual_gpu(x, fmt, rule, trial % 3)
+        want = _dual_oracle(xb, fmt, rule, trial % 3)
+        for g, w in zip(got[:4], want[:4]):
+            assert np.array_equal(g, w), (trial, rows, cols32)
+        assert got[4:] == list(want[4:]), (trial, rows, cols32)
+        # column-wise MX on a 16-column-aligned width
+        cols16 = cols32 - 16 if cols32 > 32 and trial % 4 == 1 else cols32
+        xc = x[:, :cols16].contiguous()
+        xcb = host_bits(xc)
+        q = torch.empty(rows, cols16, dtype=torch.uint8, device="cuda")
+        e8 = torch.empty(rows // 32, cols16, dtype=torch.uint8, device="cuda")
+        cl = torch.empty(1, dtype=torch.int64, device="cuda")
+        F.mx_cast_ex(xc, fmt, rule, 0, F.MX_COLWISE, q, e8, cl)
+        torch.cuda.synchronize()
+        q_o, e8_o, c_o = coracle.mx_cast_ex(xcb, fmt, rule, 0, 1)
+        assert np.array_equal(q.cpu().numpy(), q_o) and np.array_equal(e8.cpu().numpy(), e8_o), (trial, rows, cols16)
+        assert int(cl.item()) == c_o, (trial, rows, cols16)
+        # per-tensor cast + transpose, current scaling then a delayed step
+        _ct_steps((rows, cols32), dtype, fmt, 2, 2, lambda t, x=x: x * (2.0 ** (3 * t)))
+    assert F.fp8q_pipeline_status() == 0
