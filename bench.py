@@ -31,6 +31,21 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "FP8 scaled-cast GB/s (read+write) and fraction of GB300 HBM peak"
+DECODER_NAME = ("decoder_1b1 per-step cast (384 bf16 tensors, 14,092,861,440 elements; "
+                "E4M3 weights/activations, E5M2 gradients; max-window 16) + MX E4M3 OCP "
+                "cast of bf16 [16384, 8192] tanh(N(0,2))")
+
+
+def decoder_config(world: int) -> dict:
+    """The `config` of the default (decoder_1b1) bench line; the reference
+    arm reports the same one."""
+    from tensor_scaling_cast_gb300 import synthetic as S
+    cast = sum(r * c * 3 for _, (r, c), *_ in S.decoder_tensor_specs())
+    mx = 16384 * 8192 * 3 + 16384 * 8192 // 32
+    step = cast + mx
+    return {"workload": DECODER_NAME, "bytes_per_step": step, "io": "bf16/fp32 in, FP8 (+E8M0) out",
+            "l2": f"inputs larger than L2 ({step / 1e9:.2f} GB moved per step)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -180,9 +195,7 @@ class Workload:
             xs = [io_in(S.decoder_tensor(sp, 0, dev)) for sp in specs]
             grouped("grouped_cast", xs, [sp[2] for sp in specs], 16)
             mx("mx_cast", io_in(S.mx_tanh(dev)), 0)
-            self.name = ("decoder_1b1 per-step cast (384 bf16 tensors, 14,092,861,440 elements; "
-                         "E4M3 weights/activations, E5M2 gradients; max-window 16) + MX E4M3 OCP "
-                         "cast of bf16 [16384, 8192] tanh(N(0,2))")
+            self.name = DECODER_NAME
         elif kind == "grad":
             xs = [io_in(x) for x in S.grad_group_step(1, dev)]
             grouped("grouped_cast", xs, [1] * len(xs), 16)
@@ -409,8 +422,7 @@ def run_reference(args, rank: int):
             "ms_per_step": round(1e3 * elapsed / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": "decoder_1b1 per-step cast, bounded slices (see cpu_baseline)",
-                       "parallelism": "replicas"},
+            "config": decoder_config(args.gpus),
             "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": cores,
                              "kind": "oracle", "sample": desc},
             "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
