@@ -5,10 +5,12 @@
 //
 // Thread mapping: each lane owns one 16-byte load (8 bf16 or 4 fp32), so a
 // warp-wide load is 512 contiguous bytes and a 32-element block spans 4
-// (bf16) or 8 (fp32) consecutive lanes.  The block amax is an integer max of
-// abs bits finished with 2-3 xor-shuffles; E comes from the exponent field
-// (leading-bit position for subnormals).  Blocks are independent, so there
-// is no cross-CTA step besides one atomic add of the clipped count.
+// (bf16) or 8 (fp32) consecutive lanes.  The block amax is a magnitude max
+// over the lane's load (one max.NaN.xorsign.abs per pair of words, the
+// signs masked at the end) finished with 2-3 xor-shuffles; E comes from the
+// exponent field (leading-bit position for subnormals).  Blocks are
+// independent, so there is no cross-CTA step besides one atomic add of the
+// clipped count.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
