@@ -323,9 +323,10 @@ FP8Q_API int fp8q_error_stats_noalloc(const void* x, int dtype, int64_t n, const
 
 /* Number of pipeline waits on the current device that ran out of time since
  * the last call (and reset it).  Kernels that stage tiles through TMA
- * (column-wise mx_cast_ex) bound every wait for a tile; on timeout they count
- * it here and stop instead of hanging, leaving their outputs incomplete.  A
- * healthy run reads 0.  Synchronous. */
+ * (column-wise mx_cast_ex, mx_cast_dual, fp8q_cast_transpose) bound every
+ * wait for a tile; on timeout they count it here and stop instead of
+ * hanging, leaving their outputs incomplete.  A healthy run reads 0.
+ * Synchronous. */
 FP8Q_API int fp8q_pipeline_status(unsigned int* timed_out_waits);
 
 /* Diagnostic of the timeout path: one CTA waits on a pipeline barrier that
