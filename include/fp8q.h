@@ -329,10 +329,12 @@ FP8Q_API int fp8q_error_stats_noalloc(const void* x, int dtype, int64_t n, const
  * Synchronous. */
 FP8Q_API int fp8q_pipeline_status(unsigned int* timed_out_waits);
 
-/* Diagnostic of the timeout path: one CTA waits on a pipeline barrier that
- * nothing completes.  Its bounded wait gives up (after about half a second)
- * and is counted, so fp8q_pipeline_status reports one more timed-out wait;
- * the device stays usable.  One launch. */
+/* Diagnostic of the timeout path: two launches, each waiting on a pipeline
+ * barrier that nothing completes -- a bare bounded wait, and the per-warp
+ * tile pipeline of the TMA-staged kernels with no load issued.  Each wait
+ * gives up (after about half a second) and is counted, so
+ * fp8q_pipeline_status reports two more timed-out waits; the device stays
+ * usable. */
 FP8Q_API int fp8q_pipeline_selftest(void* stream);
 
 /* Name of a status code (static string). */

@@ -141,6 +141,7 @@ FP8Q_API const char* fp8q_last_cuda_error(void) { return g_cuda_err; }
 FP8Q_API int fp8q_pipeline_selftest(void* stream) {
   int launches = 0;
   cudaError_t e = launch_pipeline_selftest(reinterpret_cast<cudaStream_t>(stream), &launches);
+  if (e == cudaSuccess) e = launch_warp_pipe_selftest(reinterpret_cast<cudaStream_t>(stream), &launches);
   g_launches += launches;
   return e == cudaSuccess ? FP8Q_OK : fail_cuda(e);
 }

@@ -88,6 +88,7 @@ cudaError_t launch_stats(const void* x, int dtype, int64_t n, const uint8_t* q, 
 
 cudaError_t read_wait_timeouts(unsigned int* count);      // and reset to 0 (mx.cu)
 cudaError_t launch_pipeline_selftest(cudaStream_t s, int* launches);
+cudaError_t launch_warp_pipe_selftest(cudaStream_t s, int* launches);   // transpose.cu
 cudaError_t read_tp_wait_timeouts(unsigned int* count);   // and reset to 0 (transpose.cu)
 cudaError_t launch_mx_dual(const void* x, int dtype, int64_t rows, int64_t cols, int format, int rule,
                            int headroom, uint8_t* q_row, uint8_t* e8_row, uint8_t* q_colt,

@@ -316,6 +316,32 @@ __global__ void __launch_bounds__(kWThreads, FP8Q_TP_MINB) cast_transpose_kernel
 }
 
 // ---------------------------------------------------------------------------
+// Diagnostic of the per-warp pipeline's timeout path
+// ---------------------------------------------------------------------------
+
+// One warp sets up a pipeline over one sub-tile, initialises its barriers and
+// issues no load, so its first wait cannot complete: the bounded wait gives
+// up, counts the timeout and the warp stops (no tensor map is touched).
+__global__ void warp_pipe_selftest_kernel() {
+  using C = TpCfg<2, 1, 1, false, 2048>;
+  __shared__ __align__(8) uint64_t full[C::kStages];
+  WarpPipe<C> pipe;
+  pipe.setup(nullptr, nullptr, full, 1u, 1u, 64, &g_tp_wait_timeouts);
+  if ((threadIdx.x & 31) == 0) {
+    for (int i = 0; i < C::kStages; ++i) mbar_init(&full[i], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  pipe.wait(0);
+}
+
+cudaError_t launch_warp_pipe_selftest(cudaStream_t s, int* launches) {
+  warp_pipe_selftest_kernel<<<1, 32, 0, s>>>();
+  ++*launches;
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // launches
 // ---------------------------------------------------------------------------
 

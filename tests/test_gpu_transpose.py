@@ -195,15 +195,16 @@ def test_cast_transpose_argument_checks():
 
 
 def test_pipeline_wait_gives_up_and_is_reported():
-    """A barrier wait that nothing completes ends at its deadline, is counted
-    by fp8q_pipeline_status, and leaves the device usable."""
+    """Barrier waits that nothing completes (a bare one, and the per-warp tile
+    pipeline's own wait) end at their deadline, are counted by
+    fp8q_pipeline_status, and leave the device usable."""
     import time
     F.fp8q_pipeline_status()                          # clear
     t0 = time.time()
     F.fp8q_pipeline_selftest()
     torch.cuda.synchronize()
     assert 0.05 < time.time() - t0 < 30
-    assert F.fp8q_pipeline_status() == 1
+    assert F.fp8q_pipeline_status() == 2              # the bare wait and the per-warp pipeline
     assert F.fp8q_pipeline_status() == 0              # read resets
     x = synthetic.mx_tanh("cuda", shape=(64, 256))
     got = _dual_gpu(x, 0, 0, 0)
