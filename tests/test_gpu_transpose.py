@@ -103,10 +103,10 @@ def test_mx_dual_edge_values(dtype):
                     assert got[4:] == list(want[4:]), (rows, cols, fmt, rule, h)
 
 
-def _ct_steps(shape, dtype, fmt, window, steps, make):
+def _ct_steps(shape, dtype, fmt, window, steps, make, estimator=F.EST_MAX_WINDOW, alpha=1.0, interval=1):
     rows, cols = shape
-    h = F.fp8q_create(fmt, window, 1 if window else 0)
-    o = policy.ScalingState(fmt, window, 1 if window else 0)
+    h = F.fp8q_create_ex(fmt, window, 1 if window else 0, 0, estimator, alpha, interval)
+    o = policy.ScalingState(fmt, window, 1 if window else 0, 0, estimator, alpha, interval)
     for t in range(steps):
         x = make(t)
         q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
@@ -132,6 +132,17 @@ def test_cast_transpose_spike_sequence(window):
     current scaling (pre-pass) on step 0 or every step."""
     _ct_steps((4096, 4096), torch.bfloat16, 0, window, 12,
               lambda t: synthetic.spike_step(t, "cuda"))
+
+
+@pytest.mark.parametrize("estimator,alpha,interval", [(F.EST_SMOOTHED, 0.25, 1), (F.EST_MAX_WINDOW, 1.0, 3),
+                                                     (F.EST_SMOOTHED, 0.5, 2)])
+def test_cast_transpose_estimators(estimator, alpha, interval):
+    """The transpose takes its exponent from the same device state as the
+    grouped cast: exponential smoothing and a recompute interval over the
+    spike sequence, q, q^T, scale, amax, clipped and history each step."""
+    _ct_steps((1024, 2048), torch.bfloat16, 0, 8, 12,
+              lambda t: synthetic.spike_step(t, "cuda", shape=(1024, 2048)),
+              estimator, alpha, interval)
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
