@@ -51,13 +51,13 @@ namespace fp8q {
 #define FP8Q_CT_OBUF 2
 #endif
 #ifndef FP8Q_CT_CHUNK
-#define FP8Q_CT_CHUNK 1
+#define FP8Q_CT_CHUNK 4
 #endif
 #ifndef FP8Q_DUAL_COLF
 #define FP8Q_DUAL_COLF true
 #endif
 #ifndef FP8Q_CT_COLF
-#define FP8Q_CT_COLF false
+#define FP8Q_CT_COLF true
 #endif
 #ifndef FP8Q_TP_L2PROMO
 #define FP8Q_TP_L2PROMO 128
