@@ -29,6 +29,21 @@ def test_reference_arm_prints_one_json_line():
     assert d["cpu_baseline"]["cores"] == os.cpu_count()
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["e2e"]["value"] == d["value"]
+    import bench
+    assert d["config"] == bench.decoder_config(1)      # the same config as our arm's line
+
+
+def test_decoder_config_bytes_match_the_workload_definition():
+    """384 tensors of 3 bytes per element (2 in, 1 out) plus the MX cast of
+    bf16 [16384, 8192] at 3 + 1/32 bytes per element."""
+    import bench
+    from tensor_scaling_cast_gb300 import synthetic as S
+    specs = S.decoder_tensor_specs()
+    assert len(specs) == 384
+    n = sum(r * c for _, (r, c), *_ in specs)
+    assert n == 14_092_861_440
+    assert bench.decoder_config(1)["bytes_per_step"] == 3 * n + 3 * 16384 * 8192 + 16384 * 8192 // 32
+    assert bench.decoder_config(2)["parallelism"] == "replicas"
 
 
 def test_reference_arm_other_ranks_do_nothing():
