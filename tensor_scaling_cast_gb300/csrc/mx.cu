@@ -152,7 +152,10 @@ cudaError_t launch_mx(const void* x, int dtype, int64_t nelem, int format, int h
 #ifndef FP8Q_COL_L2PROMO
 #define FP8Q_COL_L2PROMO 128
 #endif
-using ColCfg = TpCfg<FP8Q_COL_STAGES, FP8Q_COL_OBUF, 1, FP8Q_COL_COLF, 2048>;
+#ifndef FP8Q_COL_MAXCTA
+#define FP8Q_COL_MAXCTA 0
+#endif
+using ColCfg = TpCfg<FP8Q_COL_STAGES, FP8Q_COL_OBUF, 1, FP8Q_COL_COLF, 2048, FP8Q_COL_MAXCTA>;
 
 static __device__ unsigned int g_wait_timeouts;
 
@@ -239,6 +242,7 @@ static cudaError_t launch_mx_col_t(const void* x, int64_t rows, int64_t cols, in
   int occ = 1;
   cudaError_t e = kernel_occupancy(reinterpret_cast<const void*>(kern), kWThreads, C::kSmemBytes, &occ);
   if (e != cudaSuccess) return e;
+  if (C::kMaxCtasPerSm > 0 && occ > C::kMaxCtasPerSm) occ = C::kMaxCtasPerSm;
   CUtensorMap in, qm;
   e = encode_tile_map(&in, x, DT == FP8Q_BF16, rows, cols, TILE_C, true, FP8Q_COL_L2PROMO);
   if (e == cudaSuccess) e = encode_byte_map(&qm, q, rows, cols, TILE_C, 32, TILE_C);

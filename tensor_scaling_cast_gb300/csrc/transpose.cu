@@ -34,7 +34,12 @@
 namespace fp8q {
 
 // Pipeline shape of each kernel (input stages per warp, output staging
-// buffers per warp, row tiles per chunk), overridable at build time.
+// buffers per warp, row tiles per chunk, CTAs per SM), overridable at build
+// time.  The cast + transpose moves little arithmetic per byte: it runs one
+// CTA of four warps per SM with six stages in flight per warp, which keeps
+// the read stream and its two write streams closer to the DRAM rate than
+// more, shallower warps do.  The MX dual carries much more arithmetic per
+// byte and needs the warps.
 #ifndef FP8Q_DUAL_STAGES
 #define FP8Q_DUAL_STAGES 2
 #endif
@@ -45,10 +50,16 @@ namespace fp8q {
 #define FP8Q_DUAL_CHUNK 4
 #endif
 #ifndef FP8Q_CT_STAGES
-#define FP8Q_CT_STAGES 2
+#define FP8Q_CT_STAGES 6
 #endif
 #ifndef FP8Q_CT_OBUF
-#define FP8Q_CT_OBUF 2
+#define FP8Q_CT_OBUF 1
+#endif
+#ifndef FP8Q_CT_MAXCTA
+#define FP8Q_CT_MAXCTA 1
+#endif
+#ifndef FP8Q_DUAL_MAXCTA
+#define FP8Q_DUAL_MAXCTA 0
 #endif
 #ifndef FP8Q_CT_CHUNK
 #define FP8Q_CT_CHUNK 4
@@ -65,8 +76,8 @@ namespace fp8q {
 #ifndef FP8Q_TP_MINB
 #define FP8Q_TP_MINB 4
 #endif
-using DualCfg = TpCfg<FP8Q_DUAL_STAGES, FP8Q_DUAL_OBUF, FP8Q_DUAL_CHUNK, FP8Q_DUAL_COLF, 4096>;
-using CtCfg = TpCfg<FP8Q_CT_STAGES, FP8Q_CT_OBUF, FP8Q_CT_CHUNK, FP8Q_CT_COLF, 4096>;
+using DualCfg = TpCfg<FP8Q_DUAL_STAGES, FP8Q_DUAL_OBUF, FP8Q_DUAL_CHUNK, FP8Q_DUAL_COLF, 4096, FP8Q_DUAL_MAXCTA>;
+using CtCfg = TpCfg<FP8Q_CT_STAGES, FP8Q_CT_OBUF, FP8Q_CT_CHUNK, FP8Q_CT_COLF, 4096, FP8Q_CT_MAXCTA>;
 
 static __device__ unsigned int g_tp_wait_timeouts;   // see fp8q_pipeline_status
 
@@ -356,6 +367,7 @@ static cudaError_t tp_grid(const void* kern, int64_t rows, int64_t cols, long lo
   int occ = 1;
   cudaError_t e = kernel_occupancy(kern, kWThreads, C::kSmemBytes, &occ);
   if (e != cudaSuccess) return e;
+  if (C::kMaxCtasPerSm > 0 && occ > C::kMaxCtasPerSm) occ = C::kMaxCtasPerSm;
   long long gr = (long long)sm_count(device_of_current()) * occ;
   const long long need = (nchunks + kWWarps - 1) / kWWarps;
   if (gr > need) gr = need;

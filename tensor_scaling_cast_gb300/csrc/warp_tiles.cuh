@@ -31,8 +31,9 @@ constexpr int kWTileBytes = 32 * 128;                  // 32 rows x 128 bytes
 constexpr int kWTileVec = kWTileBytes / 16;            // uint4 per sub-tile
 
 // Pipeline shape of one kernel: S input stages per warp, OB output staging
-// buffers of OUTB bytes per warp, CH row tiles per chunk, chunk order.
-template <int S, int OB, int CH, bool COLF, int OUTB>
+// buffers of OUTB bytes per warp, CH row tiles per chunk, chunk order, and
+// at most MAXC resident CTAs per SM (0: as many as fit).
+template <int S, int OB, int CH, bool COLF, int OUTB, int MAXC = 0>
 struct TpCfg {
   static_assert(S >= 2 && S <= 8, "input stages");
   static_assert(OB == 1 || OB == 2, "one or two output staging buffers");
@@ -40,6 +41,7 @@ struct TpCfg {
   static_assert(OUTB % 1024 == 0, "staging buffers keep the 1024-byte alignment of the swizzle");
   static constexpr int kStages = S, kOutBufs = OB, kChunk = CH, kOutBytes = OUTB;
   static constexpr bool kColFastest = COLF;      // chunk order: column tile fastest
+  static constexpr int kMaxCtasPerSm = MAXC;
   static constexpr int kWarpBytes = S * kWTileBytes + OB * OUTB;
   static constexpr int kSmemBytes = kWWarps * kWarpBytes + 1024;   // + alignment slack
 };
