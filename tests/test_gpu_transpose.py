@@ -103,6 +103,58 @@ def test_mx_dual_edge_values(dtype):
                     assert got[4:] == list(want[4:]), (rows, cols, fmt, rule, h)
 
 
+def _clip_boundary_tensor(rows, cols, seed):
+    """32 x 32 regions of one binade 2^k each (k from -120 to 120).  The
+    region's diagonal holds +-1.9375 * 2^k, so every row block and every
+    column block of the region has that maximum and, under the OCP rule,
+    the shared exponent k - emax_elem.  The other entries sit on the clip
+    thresholds of both formats (E4M3: 464 * 2^E = 1.8125 * 2^k, E5M2:
+    61440 * 2^E = 1.875 * 2^k), one bf16 step above and below them, or
+    well inside the range; all are exact bf16 values."""
+    rng = np.random.default_rng(seed)
+    step = 2.0 ** -7
+    pool = np.array([1.8125, 1.8125 + step, 1.8125 - step, 1.875, 1.875 + step, 1.875 - step,
+                     1.75, 1.0, 0.5, 0.0])
+    v = rng.choice(pool, size=(rows, cols)) * rng.choice([-1.0, 1.0], size=(rows, cols))
+    ks = rng.integers(-120, 121, size=(rows // 32, cols // 32))
+    v *= np.exp2(np.repeat(np.repeat(ks, 32, axis=0), 32, axis=1))
+    for i in range(rows // 32):
+        for j in range(cols // 32):
+            d = np.arange(32)
+            v[32 * i + d, 32 * j + d] = 1.9375 * 2.0 ** int(ks[i, j]) * rng.choice([-1.0, 1.0], size=32)
+    return v
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_mx_clip_boundaries(dtype):
+    """Elements exactly at, just above and just below the clip thresholds of
+    both formats: the clipped counts and bytes of the MX dual, the
+    column-wise and the row-wise MX casts equal the oracle's (every rule)."""
+    rows, cols = 128, 320
+    x = torch.from_numpy(_clip_boundary_tensor(rows, cols, 91).astype(np.float32)).to(dtype).cuda()
+    xb = host_bits(x)
+    for fmt in (0, 1):
+        for rule in (0, 1, 2):
+            got = _dual_gpu(x, fmt, rule, 0)
+            want = _dual_oracle(xb, fmt, rule, 0)
+            for g, w in zip(got[:4], want[:4]):
+                assert np.array_equal(g, w), (fmt, rule)
+            assert got[4:] == list(want[4:]), (fmt, rule)
+            if rule == 0:
+                assert got[4] > 0 and got[5] > 0          # the thresholds are crossed
+            for axis in (0, 1):
+                q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+                e8 = torch.empty((rows, cols // 32) if axis == 0 else (rows // 32, cols), dtype=torch.uint8,
+                                 device="cuda")
+                cl = torch.empty(1, dtype=torch.int64, device="cuda")
+                F.mx_cast_ex(x, fmt, rule, 0, axis, q, e8, cl)
+                torch.cuda.synchronize()
+                q_o, e8_o, c_o = coracle.mx_cast_ex(xb, fmt, rule, 0, axis, 1)
+                assert np.array_equal(q.cpu().numpy(), q_o), (fmt, rule, axis)
+                assert np.array_equal(e8.cpu().numpy(), e8_o), (fmt, rule, axis)
+                assert int(cl.item()) == c_o, (fmt, rule, axis)
+
+
 def _ct_steps(shape, dtype, fmt, window, steps, make, estimator=F.EST_MAX_WINDOW, alpha=1.0, interval=1):
     rows, cols = shape
     h = F.fp8q_create_ex(fmt, window, 1 if window else 0, 0, estimator, alpha, interval)
