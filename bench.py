@@ -213,13 +213,14 @@ class Workload:
             dq = [io_out((r, c), torch.uint8), io_out((r, c // 32), torch.uint8),
                   io_out((c, r), torch.uint8), io_out((c, r // 32), torch.uint8)]
             dcl = [torch.empty(1, dtype=torch.int64, device=dev) for _ in range(2)]
-            self.parts.append(Part("mx_cast_dual_ocp", "mx_dual_kernel",
-                                   x.numel() * (x.element_size() + 2) + 2 * (x.numel() // 32),
-                                   lambda k: F.mx_cast_dual(x, F.E4M3, 0, 0, *dq, *dcl),
-                                   lambda k: [x], lambda k: dq + dcl))
+            for nm, rule in (("mx_cast_dual_ocp", 0), ("mx_cast_dual_ceil", 1)):
+                self.parts.append(Part(nm, "mx_dual_kernel",
+                                       x.numel() * (x.element_size() + 2) + 2 * (x.numel() // 32),
+                                       lambda k, rule=rule: F.mx_cast_dual(x, F.E4M3, rule, 0, *dq, *dcl),
+                                       lambda k: [x], lambda k: dq + dcl))
             self.name = ("MX E4M3 of bf16 [16384, 8192] tanh(N(0,2)): row-wise OCP, +1 headroom, "
                          "ceil and nearest scale rules; column-wise OCP and ceil; dual (row-wise + "
-                         "transposed column-wise) OCP")
+                         "transposed column-wise) OCP and ceil")
         elif kind == "transpose":
             x = io_in(S.mx_tanh(dev))
             r, c = x.shape

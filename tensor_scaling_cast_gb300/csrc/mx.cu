@@ -155,15 +155,24 @@ cudaError_t launch_mx(const void* x, int dtype, int64_t nelem, int format, int h
 #ifndef FP8Q_COL_MAXCTA
 #define FP8Q_COL_MAXCTA 0
 #endif
+#ifndef FP8Q_COL_CLIPFREE_STAGES
+#define FP8Q_COL_CLIPFREE_STAGES 3
+#endif
+#ifndef FP8Q_COL_CLIPFREE_MAXCTA
+#define FP8Q_COL_CLIPFREE_MAXCTA 2
+#endif
+// As many CTAs as fit when blocks may clip (the exact per-element count
+// needs the warps); two CTAs of three-stage warps per SM for a clip-free
+// cast (mx_clip_free), which is memory-bound.
 using ColCfg = TpCfg<FP8Q_COL_STAGES, FP8Q_COL_OBUF, 1, FP8Q_COL_COLF, 2048, FP8Q_COL_MAXCTA>;
+using ColClipFreeCfg = TpCfg<FP8Q_COL_CLIPFREE_STAGES, FP8Q_COL_OBUF, 1, FP8Q_COL_COLF, 2048, FP8Q_COL_CLIPFREE_MAXCTA>;
 
 static __device__ unsigned int g_wait_timeouts;
 
-template <int DT, int FMT>
+template <int DT, int FMT, class C>
 __global__ void __launch_bounds__(kWThreads, 4) mx_colwise_kernel(
     const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap, int64_t rows,
     int64_t cols, uint8_t* __restrict__ e8m0, unsigned long long* clipped, int headroom, int rule) {
-  using C = ColCfg;
   constexpr int TILE_C = TileGeom<DT>::TILE_C;
   extern __shared__ __align__(1024) uint4 dyn_smem[];
   __shared__ __align__(8) uint64_t full[kWWarps][C::kStages];
@@ -230,13 +239,12 @@ __global__ void __launch_bounds__(kWThreads, 4) mx_colwise_kernel(
   if (clipped && lane == 0 && clip) atomicAdd(clipped, (unsigned long long)clip);
 }
 
-template <int DT, int FMT>
-static cudaError_t launch_mx_col_t(const void* x, int64_t rows, int64_t cols, int headroom, int rule,
+template <int DT, int FMT, class C>
+static cudaError_t launch_mx_col_c(const void* x, int64_t rows, int64_t cols, int headroom, int rule,
                                    uint8_t* q, uint8_t* e8m0, unsigned long long* clipped,
                                    cudaStream_t s, int* launches) {
-  using C = ColCfg;
   constexpr int TILE_C = TileGeom<DT>::TILE_C;
-  auto kern = mx_colwise_kernel<DT, FMT>;
+  auto kern = mx_colwise_kernel<DT, FMT, C>;
   const int64_t ctiles = (cols + TILE_C - 1) / TILE_C;
   if ((rows / 32) * ctiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // 32-bit tile counts
   int occ = 1;
@@ -254,6 +262,15 @@ static cudaError_t launch_mx_col_t(const void* x, int64_t rows, int64_t cols, in
   kern<<<(unsigned)grid, kWThreads, C::kSmemBytes, s>>>(in, qm, rows, cols, e8m0, clipped, headroom, rule);
   ++*launches;
   return cudaGetLastError();
+}
+
+template <int DT, int FMT>
+static cudaError_t launch_mx_col_t(const void* x, int64_t rows, int64_t cols, int headroom, int rule,
+                                   uint8_t* q, uint8_t* e8m0, unsigned long long* clipped, cudaStream_t s,
+                                   int* launches) {
+  return mx_clip_free(rule, headroom)
+             ? launch_mx_col_c<DT, FMT, ColClipFreeCfg>(x, rows, cols, headroom, rule, q, e8m0, clipped, s, launches)
+             : launch_mx_col_c<DT, FMT, ColCfg>(x, rows, cols, headroom, rule, q, e8m0, clipped, s, launches);
 }
 
 cudaError_t launch_mx_colwise(const void* x, int dtype, int64_t rows, int64_t cols, int format,

@@ -39,7 +39,9 @@ namespace fp8q {
 // CTA of four warps per SM with six stages in flight per warp, which keeps
 // the read stream and its two write streams closer to the DRAM rate than
 // more, shallower warps do.  The MX dual carries much more arithmetic per
-// byte and needs the warps.
+// byte when its blocks clip (the exact per-element count) and needs the
+// warps; a clip-free MX dual (mx_clip_free) runs two CTAs per SM with three
+// stages per warp.
 #ifndef FP8Q_DUAL_STAGES
 #define FP8Q_DUAL_STAGES 2
 #endif
@@ -61,6 +63,12 @@ namespace fp8q {
 #ifndef FP8Q_DUAL_MAXCTA
 #define FP8Q_DUAL_MAXCTA 0
 #endif
+#ifndef FP8Q_DUAL_CLIPFREE_STAGES
+#define FP8Q_DUAL_CLIPFREE_STAGES 3
+#endif
+#ifndef FP8Q_DUAL_CLIPFREE_MAXCTA
+#define FP8Q_DUAL_CLIPFREE_MAXCTA 2
+#endif
 #ifndef FP8Q_CT_CHUNK
 #define FP8Q_CT_CHUNK 4
 #endif
@@ -77,6 +85,8 @@ namespace fp8q {
 #define FP8Q_TP_MINB 4
 #endif
 using DualCfg = TpCfg<FP8Q_DUAL_STAGES, FP8Q_DUAL_OBUF, FP8Q_DUAL_CHUNK, FP8Q_DUAL_COLF, 4096, FP8Q_DUAL_MAXCTA>;
+using DualClipFreeCfg = TpCfg<FP8Q_DUAL_CLIPFREE_STAGES, FP8Q_DUAL_OBUF, FP8Q_DUAL_CHUNK, FP8Q_DUAL_COLF, 4096,
+                              FP8Q_DUAL_CLIPFREE_MAXCTA>;
 using CtCfg = TpCfg<FP8Q_CT_STAGES, FP8Q_CT_OBUF, FP8Q_CT_CHUNK, FP8Q_CT_COLF, 4096, FP8Q_CT_MAXCTA>;
 
 static __device__ unsigned int g_tp_wait_timeouts;   // see fp8q_pipeline_status
@@ -387,22 +397,34 @@ static cudaError_t tp_maps(const void* x, int64_t rows, int64_t cols, uint8_t* q
   return e;
 }
 
+template <int DT, int FMT, class C>
+static cudaError_t launch_dual_c(const void* x, int64_t rows, int64_t cols, int rule, int headroom,
+                                 uint8_t* q_row, uint8_t* e8_row, uint8_t* q_colt, uint8_t* e8_colt,
+                                 unsigned long long* cr, unsigned long long* cc, cudaStream_t s,
+                                 int* launches) {
+  auto kern = mx_dual_kernel<DT, FMT, C>;
+  long long grid;
+  cudaError_t e = tp_grid<DT, C>(reinterpret_cast<const void*>(kern), rows, cols, &grid);
+  if (e != cudaSuccess) return e;
+  CUtensorMap in, qm, qtm;
+  e = tp_maps<DT>(x, rows, cols, q_row, q_colt, &in, &qm, &qtm);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)grid, kWThreads, C::kSmemBytes, s>>>(in, qm, qtm, rows, cols, rule, headroom, e8_row, e8_colt,
+                                                        cr, cc);
+  ++*launches;
+  return cudaGetLastError();
+}
+
 template <int DT, int FMT>
 static cudaError_t launch_dual_t(const void* x, int64_t rows, int64_t cols, int rule, int headroom,
                                  uint8_t* q_row, uint8_t* e8_row, uint8_t* q_colt, uint8_t* e8_colt,
                                  unsigned long long* cr, unsigned long long* cc, cudaStream_t s,
                                  int* launches) {
-  auto kern = mx_dual_kernel<DT, FMT, DualCfg>;
-  long long grid;
-  cudaError_t e = tp_grid<DT, DualCfg>(reinterpret_cast<const void*>(kern), rows, cols, &grid);
-  if (e != cudaSuccess) return e;
-  CUtensorMap in, qm, qtm;
-  e = tp_maps<DT>(x, rows, cols, q_row, q_colt, &in, &qm, &qtm);
-  if (e != cudaSuccess) return e;
-  kern<<<(unsigned)grid, kWThreads, DualCfg::kSmemBytes, s>>>(in, qm, qtm, rows, cols, rule, headroom, e8_row,
-                                                              e8_colt, cr, cc);
-  ++*launches;
-  return cudaGetLastError();
+  return mx_clip_free(rule, headroom)
+             ? launch_dual_c<DT, FMT, DualClipFreeCfg>(x, rows, cols, rule, headroom, q_row, e8_row, q_colt,
+                                                       e8_colt, cr, cc, s, launches)
+             : launch_dual_c<DT, FMT, DualCfg>(x, rows, cols, rule, headroom, q_row, e8_row, q_colt, e8_colt, cr,
+                                               cc, s, launches);
 }
 
 cudaError_t launch_mx_dual(const void* x, int dtype, int64_t rows, int64_t cols, int format, int rule,

@@ -46,6 +46,14 @@ struct TpCfg {
   static constexpr int kSmemBytes = kWWarps * kWarpBytes + 1024;   // + alignment slack
 };
 
+// True when no block of an MX cast can clip: under the round-up rule the
+// scaled block maximum is at most fmax, and one or more binades of headroom
+// keep it below fmax under every rule (the E clamp only lowers it further).
+// Such casts run none of the per-element clip arithmetic, so their kernels
+// take the pipeline shape of a lighter, more memory-bound pass.  The results
+// do not depend on the shape.
+inline bool mx_clip_free(int rule, int headroom) { return rule == FP8Q_MX_CEIL || headroom >= 1; }
+
 template <int DT>
 struct TileGeom {
   static constexpr int EPL = DT == FP8Q_BF16 ? 8 : 4;   // elements per 16-byte group
