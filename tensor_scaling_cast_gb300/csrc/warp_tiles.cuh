@@ -351,8 +351,7 @@ struct OutStage {
   // Warp-collective.
   __device__ __forceinline__ void acquire() const {
     if ((threadIdx.x & 31) == 0) {
-      if (kOutBufs == 1) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-      else asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      bulk_wait_read<kOutBufs - 1>();
     }
     __syncwarp();
   }
