@@ -165,7 +165,8 @@ cudaError_t launch_mx(const void* x, int dtype, int64_t nelem, int format, int h
 // needs the warps); two CTAs of three-stage warps per SM for a clip-free
 // cast (mx_clip_free), which is memory-bound.
 using ColCfg = TpCfg<FP8Q_COL_STAGES, FP8Q_COL_OBUF, 1, FP8Q_COL_COLF, 2048, FP8Q_COL_MAXCTA>;
-using ColClipFreeCfg = TpCfg<FP8Q_COL_CLIPFREE_STAGES, FP8Q_COL_OBUF, 1, FP8Q_COL_COLF, 2048, FP8Q_COL_CLIPFREE_MAXCTA>;
+using ColClipFreeCfg =
+    TpCfg<FP8Q_COL_CLIPFREE_STAGES, FP8Q_COL_OBUF, 1, FP8Q_COL_COLF, 2048, FP8Q_COL_CLIPFREE_MAXCTA, false>;
 
 static __device__ unsigned int g_wait_timeouts;
 
@@ -202,8 +203,8 @@ __global__ void __launch_bounds__(kWThreads, 4) mx_colwise_kernel(
         load_column_words(tile, lane, w);
         const uint32_t pm = tree_absmax32<true>(w);
         uint32_t o0[8], o1[8];
-        const uint32_t e0 = mx_column<FMT, 0>(w, pm << 16, rule, headroom, clip, o0);
-        const uint32_t e1 = mx_column<FMT, 1>(w, pm & 0xFFFF0000u, rule, headroom, clip, o1);
+        const uint32_t e0 = mx_column<FMT, 0, C::kClipCount>(w, pm << 16, rule, headroom, clip, o0);
+        const uint32_t e1 = mx_column<FMT, 1, C::kClipCount>(w, pm & 0xFFFF0000u, rule, headroom, clip, o1);
 #pragma unroll
         for (int m = 0; m < 8; ++m) {               // rows 4m .. 4m + 3: (column 2l, column 2l + 1) pairs
           const uint32_t lo = __byte_perm(o0[m], o1[m], 0x5140);
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__(kWThreads, 4) mx_colwise_kernel(
       if (c < cols) {
         load_column_words(tile, lane, w);
         uint32_t o[8];
-        e8[c] = (uint8_t)mx_column<FMT, 2>(w, tree_absmax32<false>(w), rule, headroom, clip, o);
+        e8[c] = (uint8_t)mx_column<FMT, 2, C::kClipCount>(w, tree_absmax32<false>(w), rule, headroom, clip, o);
 #pragma unroll
         for (int k = 0; k < 32; ++k) ob[staged_byte<32>(k, lane)] = (uint8_t)(o[k >> 2] >> (8 * (k & 3)));
       }

@@ -86,7 +86,7 @@ namespace fp8q {
 #endif
 using DualCfg = TpCfg<FP8Q_DUAL_STAGES, FP8Q_DUAL_OBUF, FP8Q_DUAL_CHUNK, FP8Q_DUAL_COLF, 4096, FP8Q_DUAL_MAXCTA>;
 using DualClipFreeCfg = TpCfg<FP8Q_DUAL_CLIPFREE_STAGES, FP8Q_DUAL_OBUF, FP8Q_DUAL_CHUNK, FP8Q_DUAL_COLF, 4096,
-                              FP8Q_DUAL_CLIPFREE_MAXCTA>;
+                              FP8Q_DUAL_CLIPFREE_MAXCTA, false>;
 using CtCfg = TpCfg<FP8Q_CT_STAGES, FP8Q_CT_OBUF, FP8Q_CT_CHUNK, FP8Q_CT_COLF, 4096, FP8Q_CT_MAXCTA>;
 
 static __device__ unsigned int g_tp_wait_timeouts;   // see fp8q_pipeline_status
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kWThreads, FP8Q_TP_MINB) mx_dual_kernel(
         for (int k = 0; k < NG; ++k) t[k] = cast_load<DT, FMT>(v[k], s);
         pack_row<DT, NG>(t, o);
         const int be = (int)(fmax_bits(FMT) >> 23) + E;
-        if (be < 255 && m > fmax_bits(FMT) + ((uint32_t)E << 23)) {
+        if (C::kClipCount && be < 255 && m > fmax_bits(FMT) + ((uint32_t)E << 23)) {
 #pragma unroll
           for (int k = 0; k < 32; ++k)
             clip_r += clips<FMT>(__uint_as_float(elem_bits<DT>(v[k / EPL], k % EPL)) * s) ? 1u : 0u;
@@ -194,9 +194,9 @@ __global__ void __launch_bounds__(kWThreads, FP8Q_TP_MINB) mx_dual_kernel(
       if (c < cols) {
         load_column_words(tile, lane, w);
         const uint32_t pm = tree_absmax32<true>(w);
-        e8c0 |= (E8Acc<C::kChunk>)mx_column<FMT, 0>(w, pm << 16, rule, headroom, clip_c, o) << (8 * ci);
+        e8c0 |= (E8Acc<C::kChunk>)mx_column<FMT, 0, C::kClipCount>(w, pm << 16, rule, headroom, clip_c, o) << (8 * ci);
         stage32<32>(ob + 2048, 2 * lane, 0, o);
-        e8c1 |= (E8Acc<C::kChunk>)mx_column<FMT, 1>(w, pm & 0xFFFF0000u, rule, headroom, clip_c, o) << (8 * ci);
+        e8c1 |= (E8Acc<C::kChunk>)mx_column<FMT, 1, C::kClipCount>(w, pm & 0xFFFF0000u, rule, headroom, clip_c, o) << (8 * ci);
         stage32<32>(ob + 2048, 2 * lane + 1, 0, o);
         if (flush) {
           store_e8_run<C::kChunk>(e8_colt + c * rb + rt0, e8c0, ci + 1);
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kWThreads, FP8Q_TP_MINB) mx_dual_kernel(
       const int64_t c = c0 + lane;
       if (c < cols) {
         load_column_words(tile, lane, w);
-        e8c0 |= (E8Acc<C::kChunk>)mx_column<FMT, 2>(w, tree_absmax32<false>(w), rule, headroom, clip_c, o) << (8 * ci);
+        e8c0 |= (E8Acc<C::kChunk>)mx_column<FMT, 2, C::kClipCount>(w, tree_absmax32<false>(w), rule, headroom, clip_c, o) << (8 * ci);
         stage32<32>(ob + 2048, lane, 0, o);
         if (flush) store_e8_run<C::kChunk>(e8_colt + c * rb + rt0, e8c0, ci + 1);
       }

@@ -31,9 +31,11 @@ constexpr int kWTileBytes = 32 * 128;                  // 32 rows x 128 bytes
 constexpr int kWTileVec = kWTileBytes / 16;            // uint4 per sub-tile
 
 // Pipeline shape of one kernel: S input stages per warp, OB output staging
-// buffers of OUTB bytes per warp, CH row tiles per chunk, chunk order, and
-// at most MAXC resident CTAs per SM (0: as many as fit).
-template <int S, int OB, int CH, bool COLF, int OUTB, int MAXC = 0>
+// buffers of OUTB bytes per warp, CH row tiles per chunk, chunk order, at
+// most MAXC resident CTAs per SM (0: as many as fit), and whether the MX
+// kernels count clipped elements (CNT false only for clip-free casts, which
+// cannot clip).
+template <int S, int OB, int CH, bool COLF, int OUTB, int MAXC = 0, bool CNT = true>
 struct TpCfg {
   static_assert(S >= 2 && S <= 8, "input stages");
   static_assert(OB == 1 || OB == 2, "one or two output staging buffers");
@@ -42,6 +44,7 @@ struct TpCfg {
   static constexpr int kStages = S, kOutBufs = OB, kChunk = CH, kOutBytes = OUTB;
   static constexpr bool kColFastest = COLF;      // chunk order: column tile fastest
   static constexpr int kMaxCtasPerSm = MAXC;
+  static constexpr bool kClipCount = CNT;
   static constexpr int kWarpBytes = S * kWTileBytes + OB * OUTB;
   static constexpr int kSmemBytes = kWWarps * kWarpBytes + 1024;   // + alignment slack
 };
@@ -165,8 +168,11 @@ __device__ __forceinline__ int staged_byte(int k, int b) {
 }
 
 // One MX column block (column HI of the lane's words): its 32 bytes into o,
-// returns its E8M0 byte.  m = the block's max |x| bits.
-template <int FMT, int HI>
+// returns its E8M0 byte.  m = the block's max |x| bits.  With CNT the
+// block's clipped elements are added to clip (tested per element only when
+// its scaled max passes fmax); a clip-free cast (no CNT) has nothing to
+// count and carries no count code.
+template <int FMT, int HI, bool CNT>
 __device__ __forceinline__ uint32_t mx_column(const uint32_t (&w)[32], uint32_t m, int rule, int headroom,
                                               uint32_t& clip, uint32_t (&o)[8]) {
   uint32_t ebyte;
@@ -180,7 +186,7 @@ __device__ __forceinline__ uint32_t mx_column(const uint32_t (&w)[32], uint32_t 
     const float s = __uint_as_float((uint32_t)(127 - E) << 23);
     cast32<FMT, HI>(w, s, o);
     const int be = (int)(fmax_bits(FMT) >> 23) + E;
-    if (be < 255 && m > fmax_bits(FMT) + ((uint32_t)E << 23)) {
+    if (CNT && be < 255 && m > fmax_bits(FMT) + ((uint32_t)E << 23)) {
 #pragma unroll
       for (int k = 0; k < 32; ++k) clip += clips<FMT>(__uint_as_float(half_bits<HI>(w[k])) * s) ? 1u : 0u;
     }
