@@ -208,3 +208,24 @@ def test_mx_floor_rule_matches_ocp_entry(orc):
         q1, e1, c1 = orc.mx_cast(x, 0, h)
         q2, e2, c2 = orc.mx_cast_ex(x, 0, 0, h, 0)
         assert np.array_equal(q1, q2) and np.array_equal(e1, e2) and c1 == c2
+
+
+@pytest.mark.parametrize("f", [0, 1])
+def test_clip_free_rules_never_clip_any_bf16_block_max(f, orc):
+    """Every positive finite bf16 value A as a block maximum (the block holds
+    A, -A and 30 values in [0, A]): the round-up rule, and one or two binades
+    of headroom under every rule, clip nothing, while the OCP rule without
+    headroom does clip on the same blocks.  The kernels rely on this to run
+    clip-free casts without a clip count."""
+    a = np.arange(1, 0x7F80, dtype=np.uint32)             # bf16 bit patterns of every positive finite value
+    rng = np.random.default_rng(31)
+    amax = (a << 16).view(np.float32).astype(np.float64)
+    rest = amax[:, None] * rng.uniform(0.0, 1.0, size=(a.size, 30))
+    blocks = np.concatenate([amax[:, None], -amax[:, None], rest], axis=1)
+    x = _bf16(blocks)
+    assert np.array_equal(x[:, 0], a.astype(np.uint16))    # the maxima are exact
+    for rule, h in ((1, 0), (1, 1), (0, 1), (2, 1), (0, 2), (2, 2)):
+        _, _, clipped = orc.mx_cast_ex(x, f, rule, h, 0)
+        assert clipped == 0, (rule, h)
+    _, _, clipped_ocp = orc.mx_cast_ex(x, f, 0, 0, 0)
+    assert clipped_ocp > 0
