@@ -103,6 +103,35 @@ def test_mx_dual_edge_values(dtype):
                     assert got[4:] == list(want[4:]), (rows, cols, fmt, rule, h)
 
 
+@pytest.mark.parametrize("rule", [0, 1, 2])
+def test_mx_e5m2_full_size_all_layouts(rule):
+    """bf16 [16384, 8192] tanh(N(0,2)) scaled into the E5M2 range -> MX E5M2
+    row-wise, column-wise and both at once (the dual), every rule: all bytes
+    and counts equal the oracle's."""
+    x = synthetic.mx_tanh("cuda") * 3.0e4
+    xb = host_bits(x)
+    rows, cols = x.shape
+    want_r = coracle.mx_cast_ex(xb, 1, rule, 0, 0, NT)
+    want_c = coracle.mx_cast_ex(xb, 1, rule, 0, 1, NT)
+    for axis, want in ((0, want_r), (1, want_c)):
+        q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+        e8 = torch.empty((rows, cols // 32) if axis == 0 else (rows // 32, cols), dtype=torch.uint8, device="cuda")
+        cl = torch.empty(1, dtype=torch.int64, device="cuda")
+        F.mx_cast_ex(x, 1, rule, 0, axis, q, e8, cl)
+        torch.cuda.synchronize()
+        assert np.array_equal(q.cpu().numpy(), want[0]), axis
+        assert np.array_equal(e8.cpu().numpy(), want[1]), axis
+        assert int(cl.item()) == want[2], axis
+        del q, e8
+    got = _dual_gpu(x, 1, rule, 0)
+    assert np.array_equal(got[0], want_r[0]) and np.array_equal(got[1], want_r[1])
+    assert got[4] == want_r[2]
+    # the transposed column-wise layout is the row-wise MX cast of x^T
+    qc, ec, cc = coracle.mx_cast_ex(np.ascontiguousarray(xb.T), 1, rule, 0, 0, NT)
+    assert np.array_equal(got[2], qc) and np.array_equal(got[3], ec)
+    assert got[5] == cc == want_c[2]
+
+
 def _clip_boundary_tensor(rows, cols, seed):
     """32 x 32 regions of one binade 2^k each (k from -120 to 120).  The
     region's diagonal holds +-1.9375 * 2^k, so every row block and every
