@@ -60,6 +60,8 @@ def parse():
     p.add_argument("--n", type=int, default=1 << 26, help="elements for --workload single")
     p.add_argument("--single-dtype", default="bf16", choices=["bf16", "fp32"],
                    help="input type for --workload single")
+    p.add_argument("--group-policies", action="store_true",
+                   help="--workload spike: cast the step's tensor under both policies in one grouped launch")
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
@@ -140,9 +142,12 @@ class Part:
 
 
 class Workload:
-    def __init__(self, kind: str, n: int, device, host_io: bool = False, single_dtype: str = "bf16"):
+    def __init__(self, kind: str, n: int, device, host_io: bool = False, single_dtype: str = "bf16",
+                 group_policies: bool = False):
         """host_io: inputs and outputs live in pinned host memory and the
-        kernels read / write them directly over NVLink-C2C (zero-copy)."""
+        kernels read / write them directly over NVLink-C2C (zero-copy).
+        group_policies (spike): both handles cast the step's tensor in one
+        fp8q_cast_multi launch instead of one launch each."""
         import torch
 
         from tensor_scaling_cast_gb300 import fp8q as F
@@ -237,16 +242,27 @@ class Workload:
                          "[8192, 16384], max-window 16, one launch")
         elif kind == "spike":
             seq = [S.spike_step(s, dev) for s in range(S.SPIKE_STEPS)]
+            qs = []
             for name, w, m in (("most_recent_w1", 1, 0), ("max_window_w16_m1", 16, 1)):
                 g = F.ScaledCast(F.E4M3, w, m)
                 self.handles.append(g)
                 q = torch.empty(seq[0].numel(), dtype=torch.uint8, device=dev)
-                run = (lambda g, q: lambda k: g(seq[k % len(seq)], q))(g, q)
-                self.parts.append(Part(name, "cast_group_kernel", cast_bytes(seq[0]), run,
-                                       lambda k: [seq[k % len(seq)]], (lambda q: lambda k: [q])(q)))
+                qs.append(q)
+                if not group_policies:
+                    run = (lambda g, q: lambda k: g(seq[k % len(seq)], q))(g, q)
+                    self.parts.append(Part(name, "cast_group_kernel", cast_bytes(seq[0]), run,
+                                           lambda k: [seq[k % len(seq)]], (lambda q: lambda k: [q])(q)))
                 self.oracle_jobs.append(("cast", seq[0], 0, w, m))
+            if group_policies:
+                hs = [g.handle for g in self.handles]
+                outs = [torch.empty(2, dtype=torch.float32, device=dev), torch.empty(2, dtype=torch.float32, device=dev),
+                        torch.empty(2, dtype=torch.int64, device=dev)]
+                run = lambda k: F.fp8q_cast_multi(hs, [seq[k % len(seq)]] * 2, qs, *outs)
+                self.parts.append(Part("both_policies_grouped", "cast_group_kernel", 2 * cast_bytes(seq[0]), run,
+                                       lambda k: [seq[k % len(seq)]], lambda k: qs + outs))
             self.name = ("spike_seq: bf16 [4096, 4096] E4M3, inputs rotating over the 16 steps "
-                         "(512 MiB), most-recent and max-window-16 (margin 1) per step")
+                         "(512 MiB), most-recent and max-window-16 (margin 1) per step"
+                         + (", both policies in one grouped launch" if group_policies else ""))
         elif kind == "current":
             x = S.current_4096(dev)
             g = F.ScaledCast(F.E4M3, 0, 0)
@@ -450,7 +466,7 @@ def run_ours(args, rank: int, world: int):
     if world > 1:
         dist.barrier()
     F.load()
-    W = Workload(args.workload, args.n, dev, single_dtype=args.single_dtype)
+    W = Workload(args.workload, args.n, dev, single_dtype=args.single_dtype, group_policies=args.group_policies)
     torch.cuda.synchronize()
     clocks = Clocks(local)
     clocks.start()
@@ -725,7 +741,8 @@ def run_e2e_zero_copy(args, world: int, dev):
     straight to the C ABI: the kernels read the inputs and write the
     results over NVLink-C2C, so each step moves the same host bytes."""
     import torch
-    W = Workload(args.workload, args.n, dev, host_io=True, single_dtype=args.single_dtype)
+    W = Workload(args.workload, args.n, dev, host_io=True, single_dtype=args.single_dtype,
+                 group_policies=args.group_policies)
     for k in range(3):
         W.step(k)
     torch.cuda.synchronize()
