@@ -131,8 +131,9 @@ FP8Q_API int fp8q_create_ex(int format, int window, int margin_bits, int hystere
 
 /* Read / restore the estimator state that fp8q_set_history does not cover:
  * the running average (valid when *has_average) and the number of casts
- * done (the phase of the recompute interval).  Both block until the
- * handle's last cast has finished. */
+ * done (the phase of the recompute interval).  Setting it leaves the window
+ * and the previous exponent as they are.  Both block until the handle's
+ * last cast has finished. */
 FP8Q_API int fp8q_get_estimator_state(fp8q_handle h, float* average, int* has_average,
                                       long long* steps);
 FP8Q_API int fp8q_set_estimator_state(fp8q_handle h, float average, int has_average,
@@ -142,8 +143,14 @@ FP8Q_API int fp8q_set_estimator_state(fp8q_handle h, float average, int has_aver
  * NULL is accepted (returns FP8Q_OK). */
 FP8Q_API int fp8q_destroy(fp8q_handle h);
 
-/* Fused scaled cast of one tensor (steps: amax reduction, scale from the
- * window, saturating RNE cast with clipped count, cross-CTA finish).
+/* Fused scaled cast of one tensor ("Practice c06/E3", worked solution: the
+ * largest |x| of the tensor watched over a window of steps sets a
+ * power-of-two scale; "Mixed Precision FP16/BF16/FP8" mind-map card, bit
+ * layouts and ranges: E4M3 max 448, E5M2 max 57344; gist.science summary of
+ * "Max-Window Scale Estimation ...", Methodology: the delayed estimators use
+ * historical amaxes, current scaling a second pass).  Steps: amax reduction,
+ * scale from the window, saturating RNE cast with clipped count, cross-CTA
+ * finish.
  *   x       device, n elements of `dtype` (FP8Q_F32 or FP8Q_BF16), 16-B aligned
  *   n       >= 0 elements (any n; n = 0 records amax 0)
  *   q       device, n bytes out (the handle's format), 16-B aligned
@@ -156,7 +163,12 @@ FP8Q_API int fp8q_cast(fp8q_handle h, const void* x, int dtype, int64_t n, uint8
                        void* stream);
 
 /* Grouped version of fp8q_cast over `count` tensors in one launch (plus one
- * amax pre-pass launch if any tensor needs current scaling).  hs, xs,
+ * amax pre-pass launch if any tensor needs current scaling).  Each tensor
+ * keeps its own statistic and scale ("Practice c06/E3", worked solution:
+ * the scale is set per tensor rather than per run; gist.science summary of
+ * "Max-Window Scale Estimation ...", Methodology, Quantization
+ * Configuration: W8A8 casts the weights and the activations of the gate, up
+ * and down projections of many blocks at every step).  hs, xs,
  * dtypes, ns, qs are HOST arrays of length count (xs/qs hold device
  * pointers); the handles must be distinct.  d_scale_inv, d_amax, d_clipped
  * are DEVICE arrays of length count (or NULL).  Work is split into equal
@@ -260,8 +272,12 @@ FP8Q_API int mx_cast_dual(const void* x, int dtype, int64_t rows, int64_t cols, 
                           uint8_t* e8m0_colt, unsigned long long* d_clipped_row,
                           unsigned long long* d_clipped_col, void* stream);
 
-/* Read a handle's amax history (oldest first) to host memory.  Blocks until
- * the handle's last cast has finished.  capacity must be >= the window;
+/* Read a handle's amax history (oldest first) to host memory ("Practice
+ * c06/E3", worked solution: the window of past largest |x| values the scale
+ * comes from; gist.science summary of "Max-Window Scale Estimation ...",
+ * Methodology: the history is filled during a BF16 warm-up, so it is
+ * training state worth saving).  Blocks until the handle's last cast has
+ * finished.  capacity must be >= the window;
  * *n_valid receives the number of entries written. */
 FP8Q_API int fp8q_amax_history(fp8q_handle h, float* host_out, int capacity, int* n_valid);
 
@@ -270,12 +286,19 @@ FP8Q_API int fp8q_amax_history(fp8q_handle h, float* host_out, int capacity, int
  * pointer may be NULL. */
 FP8Q_API int fp8q_scale_state(fp8q_handle h, int* prev_exp, long long* steps);
 
-/* Restore a handle's state (resume from a checkpoint): n (<= window) amax
- * values, oldest first, and the previous exponent (FP8Q_NO_EXP for none).
- * Blocks until the handle's last cast has finished. */
+/* Restore a handle's window (resume from a checkpoint; "Practice c06/E3",
+ * worked solution: the window and the previous scale that hysteresis keeps;
+ * gist.science summary of "Max-Window Scale Estimation ...", Methodology: a
+ * history filled before quantising): n (<= window) amax values, oldest
+ * first, and the previous exponent (FP8Q_NO_EXP for none).  Only the window
+ * and the previous exponent change: the estimator state of
+ * fp8q_set_estimator_state (running average, number of casts, interval
+ * phase) is kept, so the two restores may come in either order.  Blocks
+ * until the handle's last cast has finished. */
 FP8Q_API int fp8q_set_history(fp8q_handle h, const float* host_in, int n, int prev_exp);
 
-/* Clear a handle's history and previous exponent (as after fp8q_create). */
+/* Clear a handle's history, previous exponent and estimator state (as after
+ * fp8q_create). */
 FP8Q_API int fp8q_reset(fp8q_handle h);
 
 /* Dequantised-error statistics of a per-tensor cast, over the elements whose
@@ -311,7 +334,10 @@ FP8Q_API int mx_error_stats(const void* x, int dtype, int64_t rows, int64_t cols
  *   by every GPU that loads the library until the process exits.
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is looked up again only when
+ *   the device's context has been re-created (after a cudaDeviceReset).
+ *   One CTA per row of the array: 4 per SM, or one per 2^20 elements when
+ *   that is more.
  *   All calls share the one array, which keeps the contents of the last
  *   call: calls that overlap on the GPU (two streams, or two host threads)
  *   race on it and give wrong results, so order them on one stream. */

@@ -139,6 +139,7 @@ FP8Q_API const char* fp8q_strerror(int code) {
 FP8Q_API const char* fp8q_last_cuda_error(void) { return g_cuda_err; }
 
 FP8Q_API int fp8q_pipeline_selftest(void* stream) {
+  FP8Q_TRACE_CALL();
   int launches = 0;
   cudaError_t e = launch_pipeline_selftest(reinterpret_cast<cudaStream_t>(stream), &launches);
   if (e == cudaSuccess) e = launch_warp_pipe_selftest(reinterpret_cast<cudaStream_t>(stream), &launches);
@@ -147,6 +148,7 @@ FP8Q_API int fp8q_pipeline_selftest(void* stream) {
 }
 
 FP8Q_API int fp8q_pipeline_status(unsigned int* timed_out_waits) {
+  FP8Q_TRACE_CALL();
   if (!timed_out_waits) return FP8Q_EINVAL;
   unsigned int a = 0, b = 0;
   cudaError_t e = read_wait_timeouts(&a);
@@ -159,6 +161,7 @@ FP8Q_API long long fp8q_launch_count(void) { return g_launches.load(); }
 
 FP8Q_API int fp8q_create_ex(int format, int window, int margin_bits, int hysteresis_bits,
                             int estimator, float alpha, int interval, fp8q_handle* out) {
+  FP8Q_TRACE_CALL();
   if (!out) return FP8Q_EINVAL;
   *out = nullptr;
   if (!format_ok(format)) return FP8Q_EDTYPE;
@@ -202,11 +205,13 @@ FP8Q_API int fp8q_create_ex(int format, int window, int margin_bits, int hystere
 
 FP8Q_API int fp8q_create(int format, int window, int margin_bits, int hysteresis_bits,
                          fp8q_handle* out) {
+  FP8Q_TRACE_CALL();
   return fp8q_create_ex(format, window, margin_bits, hysteresis_bits, FP8Q_EST_MAX_WINDOW, 1.0f,
                         1, out);
 }
 
 FP8Q_API int fp8q_destroy(fp8q_handle h) {
+  FP8Q_TRACE_CALL();
   if (h == nullptr) return FP8Q_OK;
   if (!handle_ok(h)) return FP8Q_EHANDLE;
   int dev = 0;
@@ -302,6 +307,7 @@ static int check_tensor(fp8q_handle h, const void* x, int dtype, int64_t n, cons
 FP8Q_API int fp8q_cast(fp8q_handle h, const void* x, int dtype, int64_t n, uint8_t* q,
                        float* d_scale_inv, float* d_amax, unsigned long long* d_clipped,
                        void* stream) {
+  FP8Q_TRACE_CALL();
   int st = check_tensor(h, x, dtype, n, q);
   if (st != FP8Q_OK) return st;
   st = check_device(h);
@@ -315,6 +321,7 @@ FP8Q_API int fp8q_cast_multi_ex(const fp8q_handle* hs, const void* const* xs, co
                                 float* d_amax, unsigned long long* d_clipped,
                                 unsigned long long* d_nonfinite, unsigned long long* d_underflow,
                                 int count, void* stream) {
+  FP8Q_TRACE_CALL();
   if (count <= 0 || !hs || !xs || !dtypes || !ns || !qs) return FP8Q_EINVAL;
   for (int i = 0; i < count; ++i) {
     int st = check_tensor(hs[i], xs[i], dtypes[i], ns[i], qs[i]);
@@ -333,6 +340,7 @@ FP8Q_API int fp8q_cast_multi(const fp8q_handle* hs, const void* const* xs, const
                              const int64_t* ns, uint8_t* const* qs, float* d_scale_inv,
                              float* d_amax, unsigned long long* d_clipped, int count,
                              void* stream) {
+  FP8Q_TRACE_CALL();
   return fp8q_cast_multi_ex(hs, xs, dtypes, ns, qs, d_scale_inv, d_amax, d_clipped, nullptr, nullptr,
                             count, stream);
 }
@@ -353,6 +361,7 @@ extern "C" {
 
 FP8Q_API int fp8q_loss_scaler_create(float init_scale, int growth_interval, float min_scale,
                                      float max_scale, fp8q_loss_scaler* out) {
+  FP8Q_TRACE_CALL();
   if (!out) return FP8Q_EINVAL;
   *out = nullptr;
   if (!(min_scale > 0.0f) || !(max_scale >= min_scale) || !(init_scale >= min_scale) ||
@@ -380,6 +389,7 @@ FP8Q_API int fp8q_loss_scaler_create(float init_scale, int growth_interval, floa
 }
 
 FP8Q_API int fp8q_loss_scaler_destroy(fp8q_loss_scaler ls) {
+  FP8Q_TRACE_CALL();
   if (!ls) return FP8Q_OK;
   if (ls->magic != kScalerMagic) return FP8Q_EHANDLE;
   if (ls->has_last) cudaEventSynchronize(ls->last);
@@ -392,6 +402,7 @@ FP8Q_API int fp8q_loss_scaler_destroy(fp8q_loss_scaler ls) {
 
 FP8Q_API int fp8q_loss_scaler_update(fp8q_loss_scaler ls, const unsigned long long* d_nonfinite,
                                      int count, float* d_scale, int* d_skip, void* stream) {
+  FP8Q_TRACE_CALL();
   if (!ls || ls->magic != kScalerMagic) return FP8Q_EHANDLE;
   if (count < 0 || (count > 0 && !d_nonfinite)) return FP8Q_EINVAL;
   int dev = 0;
@@ -410,6 +421,7 @@ FP8Q_API int fp8q_loss_scaler_update(fp8q_loss_scaler ls, const unsigned long lo
 }
 
 FP8Q_API int fp8q_loss_scaler_read(fp8q_loss_scaler ls, float* scale, int* good_steps) {
+  FP8Q_TRACE_CALL();
   if (!ls || ls->magic != kScalerMagic) return FP8Q_EHANDLE;
   if (ls->has_last) {
     cudaError_t e = cudaEventSynchronize(ls->last);
@@ -426,6 +438,7 @@ FP8Q_API int fp8q_loss_scaler_read(fp8q_loss_scaler ls, float* scale, int* good_
 FP8Q_API int mx_cast_ex(const void* x, int dtype, int64_t rows, int64_t cols, int format,
                         int rule, int headroom_bits, int axis, uint8_t* q, uint8_t* e8m0,
                         unsigned long long* d_clipped, void* stream) {
+  FP8Q_TRACE_CALL();
   if (!dtype_ok(dtype) || !format_ok(format)) return FP8Q_EDTYPE;
   if (rule < FP8Q_MX_FLOOR || rule > FP8Q_MX_NEAREST) return FP8Q_EINVAL;
   if (axis != FP8Q_MX_ROWWISE && axis != FP8Q_MX_COLWISE) return FP8Q_EINVAL;
@@ -455,6 +468,7 @@ FP8Q_API int mx_cast_dual(const void* x, int dtype, int64_t rows, int64_t cols, 
                           int headroom_bits, uint8_t* q_row, uint8_t* e8m0_row, uint8_t* q_colt,
                           uint8_t* e8m0_colt, unsigned long long* d_clipped_row,
                           unsigned long long* d_clipped_col, void* stream) {
+  FP8Q_TRACE_CALL();
   if (!dtype_ok(dtype) || !format_ok(format)) return FP8Q_EDTYPE;
   if (rule < FP8Q_MX_FLOOR || rule > FP8Q_MX_NEAREST) return FP8Q_EINVAL;
   if (rows < 0 || cols <= 0 || rows % 32 != 0 || cols % 32 != 0 || headroom_bits < 0 ||
@@ -482,6 +496,7 @@ FP8Q_API int mx_cast_dual(const void* x, int dtype, int64_t rows, int64_t cols, 
 FP8Q_API int fp8q_cast_transpose(fp8q_handle h, const void* x, int dtype, int64_t rows, int64_t cols,
                                  uint8_t* q, uint8_t* qt, float* d_scale_inv, float* d_amax,
                                  unsigned long long* d_clipped, void* stream) {
+  FP8Q_TRACE_CALL();
   if (!handle_ok(h)) return FP8Q_EHANDLE;
   if (!dtype_ok(dtype)) return FP8Q_EDTYPE;
   if (rows <= 0 || cols <= 0 || rows % 32 != 0 || cols % 32 != 0) return FP8Q_EINVAL;
@@ -531,11 +546,13 @@ FP8Q_API int fp8q_cast_transpose(fp8q_handle h, const void* x, int dtype, int64_
 FP8Q_API int mx_cast(const void* x, int dtype, int64_t rows, int64_t cols, int format,
                      int headroom_bits, uint8_t* q, uint8_t* e8m0,
                      unsigned long long* d_clipped, void* stream) {
+  FP8Q_TRACE_CALL();
   return mx_cast_ex(x, dtype, rows, cols, format, FP8Q_MX_FLOOR, headroom_bits, FP8Q_MX_ROWWISE,
                     q, e8m0, d_clipped, stream);
 }
 
 FP8Q_API int fp8q_amax_history(fp8q_handle h, float* host_out, int capacity, int* n_valid) {
+  FP8Q_TRACE_CALL();
   if (!handle_ok(h)) return FP8Q_EHANDLE;
   if (!n_valid || (capacity > 0 && !host_out) || capacity < h->window) return FP8Q_EINVAL;
   int st = check_device(h);
@@ -555,6 +572,7 @@ FP8Q_API int fp8q_amax_history(fp8q_handle h, float* host_out, int capacity, int
 }
 
 FP8Q_API int fp8q_scale_state(fp8q_handle h, int* prev_exp, long long* steps) {
+  FP8Q_TRACE_CALL();
   if (!handle_ok(h)) return FP8Q_EHANDLE;
   int st = check_device(h);
   if (st == FP8Q_OK) st = wait_last(h);
@@ -567,10 +585,20 @@ FP8Q_API int fp8q_scale_state(fp8q_handle h, int* prev_exp, long long* steps) {
   return FP8Q_OK;
 }
 
-static int write_state(fp8q_handle h, const float* host_in, int n, int prev_exp, long long steps) {
+// Write a handle's window (n values, oldest first) and previous exponent.
+// keep_estimator: the running average, the number of casts and the interval
+// phase are read back and kept (a restore of the window alone); otherwise
+// they are cleared with everything else (a reset).
+static int write_state(fp8q_handle h, const float* host_in, int n, int prev_exp, bool keep_estimator) {
   int st = check_device(h);
   if (st == FP8Q_OK) st = wait_last(h);
   if (st != FP8Q_OK) return st;
+  DevState old;
+  std::memset(&old, 0, sizeof old);
+  if (keep_estimator) {
+    cudaError_t e = cudaMemcpy(&old, h->dev, sizeof old, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
   DevState d;
   std::memset(&d, 0, sizeof d);
   d.format = h->format;
@@ -590,17 +618,20 @@ static int write_state(fp8q_handle h, const float* host_in, int n, int prev_exp,
   d.head = (h->window > 0) ? n % h->window : 0;
   d.has_prev = prev_exp != FP8Q_NO_EXP;
   d.prev_e = d.has_prev ? prev_exp : 0;
-  d.steps = steps;
-  d.phase = (int32_t)(steps % h->interval);
+  d.steps = old.steps;
+  d.phase = old.phase;
+  d.avg = old.avg;
+  d.has_avg = old.has_avg;
   cudaError_t e = cudaMemcpy(h->dev, &d, sizeof d, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return fail_cuda(e);
   h->host_count = n;
-  h->host_casts = steps;
+  h->host_casts = d.steps;
   return FP8Q_OK;
 }
 
 FP8Q_API int fp8q_get_estimator_state(fp8q_handle h, float* average, int* has_average,
                                       long long* steps) {
+  FP8Q_TRACE_CALL();
   if (!handle_ok(h)) return FP8Q_EHANDLE;
   int st = check_device(h);
   if (st == FP8Q_OK) st = wait_last(h);
@@ -616,6 +647,7 @@ FP8Q_API int fp8q_get_estimator_state(fp8q_handle h, float* average, int* has_av
 
 FP8Q_API int fp8q_set_estimator_state(fp8q_handle h, float average, int has_average,
                                       long long steps) {
+  FP8Q_TRACE_CALL();
   if (!handle_ok(h)) return FP8Q_EHANDLE;
   if (steps < 0) return FP8Q_EINVAL;
   int st = check_device(h);
@@ -635,19 +667,22 @@ FP8Q_API int fp8q_set_estimator_state(fp8q_handle h, float average, int has_aver
 }
 
 FP8Q_API int fp8q_set_history(fp8q_handle h, const float* host_in, int n, int prev_exp) {
+  FP8Q_TRACE_CALL();
   if (!handle_ok(h)) return FP8Q_EHANDLE;
   if (n < 0 || n > h->window || (n > 0 && !host_in)) return FP8Q_EINVAL;
   if (prev_exp != FP8Q_NO_EXP && (prev_exp < -126 || prev_exp > 126)) return FP8Q_EINVAL;
-  return write_state(h, host_in, n, prev_exp, 0);
+  return write_state(h, host_in, n, prev_exp, true);
 }
 
 FP8Q_API int fp8q_reset(fp8q_handle h) {
+  FP8Q_TRACE_CALL();
   if (!handle_ok(h)) return FP8Q_EHANDLE;
-  return write_state(h, nullptr, 0, FP8Q_NO_EXP, 0);
+  return write_state(h, nullptr, 0, FP8Q_NO_EXP, false);
 }
 
 FP8Q_API int fp8q_error_stats(const void* x, int dtype, int64_t n, const uint8_t* q, int format,
                               const float* d_scale_inv, double* d_out, void* stream) {
+  FP8Q_TRACE_CALL();
   if (!dtype_ok(dtype) || !format_ok(format)) return FP8Q_EDTYPE;
   if (n < 0 || !d_out || !d_scale_inv || (n > 0 && (!x || !q))) return FP8Q_EINVAL;
   int launches = 0;
@@ -660,6 +695,7 @@ FP8Q_API int fp8q_error_stats(const void* x, int dtype, int64_t n, const uint8_t
 FP8Q_API int mx_error_stats(const void* x, int dtype, int64_t rows, int64_t cols,
                             const uint8_t* q, const uint8_t* e8m0, int format, double* d_out,
                             void* stream) {
+  FP8Q_TRACE_CALL();
   if (!dtype_ok(dtype) || !format_ok(format)) return FP8Q_EDTYPE;
   if (rows < 0 || cols <= 0 || cols % 32 != 0 || !d_out) return FP8Q_EINVAL;
   const int64_t n = rows * cols;

@@ -3,11 +3,34 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "fp8q.h"
 
 namespace fp8q {
+
+// NVTX range over one C-ABI call, named after the entry point, in the
+// library's own "fp8q" domain.  With no tool attached NVTX's entry points
+// return at once, so the range costs a call and a branch.
+inline nvtxDomainHandle_t trace_domain() {
+  static const nvtxDomainHandle_t d = nvtxDomainCreateA("fp8q");
+  return d;
+}
+struct TraceRange {
+  explicit TraceRange(const char* name) {
+    nvtxEventAttributes_t a = {};
+    a.version = NVTX_VERSION;
+    a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+    a.message.ascii = name;
+    nvtxDomainRangePushEx(trace_domain(), &a);
+  }
+  ~TraceRange() { nvtxDomainRangePop(trace_domain()); }
+  TraceRange(const TraceRange&) = delete;
+  TraceRange& operator=(const TraceRange&) = delete;
+};
+#define FP8Q_TRACE_CALL() ::fp8q::TraceRange fp8q_trace_range_(__func__)
 
 constexpr int kThreads = 256;                 // threads per CTA (8 warps)
 constexpr int kUnroll = 8;                    // 16-byte loads in flight per thread

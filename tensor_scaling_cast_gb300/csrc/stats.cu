@@ -8,8 +8,11 @@
 // Differences and squares are formed in fp64.  Each CTA writes its partial
 // sums to a scratch row; a one-CTA kernel adds the rows in index order, so the
 // result does not depend on scheduling.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "fp8q_device.cuh"
@@ -140,9 +143,13 @@ cudaError_t launch_stats(const void* x, int dtype, int64_t n, const uint8_t* q, 
 // statistics (their own allocator owns the device's memory, they run after
 // an out-of-memory error, or an allocation would stall a latency-bound
 // loop).  The per-CTA partial sums go to this fixed array instead of a
-// cudaMallocAsync block: one CTA per slab of 2^20 elements, one row of three
-// doubles per CTA, so n <= 4096 * 2^20.  Every row the final kernel reads is
-// written earlier in the same call, so nothing needs clearing between calls.
+// cudaMallocAsync block, one row of three doubles per CTA.  The grid is the
+// allocating variant's (4 CTAs per SM), raised to one CTA per 2^20 elements
+// for larger tensors, and never above the array's 4096 rows: each CTA
+// grid-strides over the tensor, so n <= 4096 * 2^20 keeps a CTA's share at
+// most 2^20 elements.  Every row the final kernel reads (rows 0 .. grid-1)
+// is written earlier in the same call, so nothing needs clearing between
+// calls.
 namespace fp8q {
 
 constexpr int kNoAllocRows = FP8Q_STATS_NOALLOC_ROWS;
@@ -151,21 +158,53 @@ static_assert(FP8Q_STATS_NOALLOC_MAX_N == kNoAllocRows * kNoAllocSlab, "limit an
 
 static __device__ __align__(256) double g_stats_scratch[3 * kNoAllocRows];
 
-// Device address of g_stats_scratch for each device, looked up once with
-// that device current (the host-side name is only a stand-in).
+// Device address of g_stats_scratch for each device (the host-side name is
+// only a stand-in), looked up with that device current on the first call,
+// and again when the device's context is no longer the one the address was
+// taken in (a caller's cudaDeviceReset re-creates the context and reloads
+// the module, which moves the array).  Contexts are told apart by the
+// driver's per-process unique context id.
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  double* ptr;
+};
 static std::mutex g_scratch_mu;
-static double* g_scratch_ptr[128] = {};
+static ScratchEntry g_scratch[128] = {};
+
+static unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  unsigned long long id = 0;
+  return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
 
 static cudaError_t stats_scratch(int device, double** out) {
   if (device < 0 || device >= 128) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (g_scratch_ptr[device] == nullptr) {
+  ScratchEntry& en = g_scratch[device];
+  const unsigned long long id = current_context_id();
+  if (en.ptr == nullptr || id == 0 || id != en.ctx_id) {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_stats_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_stats_scratch);   // makes the context current
     if (e != cudaSuccess) return e;
-    g_scratch_ptr[device] = static_cast<double*>(p);
+    en.ptr = static_cast<double*>(p);
+    en.ctx_id = current_context_id();
   }
-  *out = g_scratch_ptr[device];
+  *out = en.ptr;
   return cudaSuccess;
 }
 
@@ -175,6 +214,7 @@ extern "C" FP8Q_API int fp8q_error_stats_noalloc(const void* x, int dtype, int64
                                                  const uint8_t* q, int format,
                                                  const float* d_scale_inv, double* d_out,
                                                  void* stream) {
+  FP8Q_TRACE_CALL();
   using namespace fp8q;
   if (dtype != FP8Q_F32 && dtype != FP8Q_BF16) return FP8Q_EDTYPE;
   if (format != FP8Q_E4M3 && format != FP8Q_E5M2) return FP8Q_EDTYPE;
@@ -188,7 +228,9 @@ extern "C" FP8Q_API int fp8q_error_stats_noalloc(const void* x, int dtype, int64
   double* partial = nullptr;
   cudaError_t e = stats_scratch(device_of_current(), &partial);
   if (e != cudaSuccess) return record_cuda_error(e);
-  const int grid = (int)((n + kNoAllocSlab - 1) / kNoAllocSlab);
+  const int64_t slabs = (n + kNoAllocSlab - 1) / kNoAllocSlab;
+  const int grid = (int)std::min<int64_t>(
+      kNoAllocRows, std::max<int64_t>(slabs, (int64_t)sm_count(device_of_current()) * 4));
   const int key = (dtype == FP8Q_BF16 ? 1 : 0) | (format == FP8Q_E5M2 ? 2 : 0);
   switch (key) {
     case 0: launch_partial<FP8Q_F32, FP8Q_E4M3, false>(x, n, q, d_scale_inv, nullptr, partial, grid, s); break;

@@ -30,6 +30,7 @@ def test_reference_arm_prints_one_json_line():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["e2e"]["value"] == d["value"]
     import bench
+    assert d["dtype"] == bench.DTYPE
     assert d["config"] == bench.decoder_config(1)      # the same config as our arm's line
 
 
@@ -81,3 +82,24 @@ def test_max_over_ranks_gloo_world2():
 def test_max_over_ranks_single_process_is_identity():
     import bench
     assert bench.max_over_ranks(3.25, 1, "cpu") == 3.25
+
+
+def test_input_digests_are_sha256_of_each_tensors_bytes():
+    """inputs_sha256 of a bench line: the SHA-256 of each input tensor's raw
+    bytes, keyed by the tensor's name (bf16 and fp32, one tensor larger
+    than the 2^26-element hashing stride)."""
+    import hashlib
+    import types
+
+    import bench
+    g = torch.Generator().manual_seed(3)
+    a = torch.randn(1000, generator=g).to(torch.bfloat16)
+    b = torch.randn((1 << 26) + 7, generator=g)
+    d = bench.input_digests(types.SimpleNamespace(named_inputs=[("a", a), ("b", b)]))
+    assert d == {"a": hashlib.sha256(a.view(torch.int16).numpy().tobytes()).hexdigest(),
+                 "b": hashlib.sha256(b.numpy().tobytes()).hexdigest()}
+
+
+def test_lines_name_the_arithmetic_not_just_a_float_type():
+    import bench
+    assert "bf16" in bench.DTYPE and "fp8" in bench.DTYPE and "fp32" in bench.DTYPE

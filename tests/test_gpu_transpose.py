@@ -4,6 +4,8 @@ fp8q_cast_transpose: q must equal the oracle's per-tensor cast of x and qt
 its transpose; amax, scale_inv, clipped and the history as for fp8q_cast.
 mx_cast_dual: (q_row, e8m0_row) must equal the oracle's row-wise MX cast of
 x and (q_colt, e8m0_colt) the row-wise MX cast of x^T.  All bit-exact.
+Every output buffer carries guard bands (tests/canary.py) of at least one
+32-row tile-store box on each side, checked after every call.
 """
 import os
 
@@ -11,11 +13,14 @@ import numpy as np
 import pytest
 import torch
 
+from canary import Guards
 from oracle import coracle, policy
 from tensor_scaling_cast_gb300 import fp8q as F
 from tensor_scaling_cast_gb300 import synthetic
 
 pytestmark = pytest.mark.gpu
+
+G = Guards(seed=0x7A9)
 
 NT = os.cpu_count() or 1
 
@@ -28,6 +33,13 @@ def _lib():
     build.build()
     F.load()
     torch.cuda.set_device(0)
+
+
+@pytest.fixture(autouse=True)
+def _guards():
+    G.release()
+    yield
+    G.check_and_release("at the end of the test")
 
 
 def host_bits(x: torch.Tensor) -> np.ndarray:
@@ -56,16 +68,18 @@ def _edge_tensor(rows, cols, dtype, seed):
 
 def _dual_gpu(x, fmt, rule, headroom):
     rows, cols = x.shape
-    qr = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
-    er = torch.empty(rows, cols // 32, dtype=torch.uint8, device="cuda")
-    qc = torch.empty(cols, rows, dtype=torch.uint8, device="cuda")
-    ec = torch.empty(cols, rows // 32, dtype=torch.uint8, device="cuda")
-    cr = torch.empty(1, dtype=torch.int64, device="cuda")
-    cc = torch.empty(1, dtype=torch.int64, device="cuda")
+    qr = G.empty((rows, cols), torch.uint8)
+    er = G.empty((rows, cols // 32), torch.uint8)
+    qc = G.empty((cols, rows), torch.uint8)
+    ec = G.empty((cols, rows // 32), torch.uint8)
+    cr = G.empty(1, torch.int64)
+    cc = G.empty(1, torch.int64)
     F.mx_cast_dual(x, fmt, rule, headroom, qr, er, qc, ec, cr, cc)
-    torch.cuda.synchronize()
+    G.check(f"mx_cast_dual {rows}x{cols} fmt={fmt} rule={rule} h={headroom}")
     assert F.fp8q_pipeline_status() == 0
-    return [t.cpu().numpy() for t in (qr, er, qc, ec)] + [int(cr.item()), int(cc.item())]
+    out = [t.cpu().numpy() for t in (qr, er, qc, ec)] + [int(cr.item()), int(cc.item())]
+    G.release()
+    return out
 
 
 def _dual_oracle(xb, fmt, rule, headroom, nthreads=1):
@@ -114,14 +128,15 @@ def test_mx_e5m2_full_size_all_layouts(rule):
     want_r = coracle.mx_cast_ex(xb, 1, rule, 0, 0, NT)
     want_c = coracle.mx_cast_ex(xb, 1, rule, 0, 1, NT)
     for axis, want in ((0, want_r), (1, want_c)):
-        q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
-        e8 = torch.empty((rows, cols // 32) if axis == 0 else (rows // 32, cols), dtype=torch.uint8, device="cuda")
-        cl = torch.empty(1, dtype=torch.int64, device="cuda")
+        q = G.empty((rows, cols), torch.uint8)
+        e8 = G.empty((rows, cols // 32) if axis == 0 else (rows // 32, cols), torch.uint8)
+        cl = G.empty(1, torch.int64)
         F.mx_cast_ex(x, 1, rule, 0, axis, q, e8, cl)
-        torch.cuda.synchronize()
+        G.check(f"axis {axis}")
         assert np.array_equal(q.cpu().numpy(), want[0]), axis
         assert np.array_equal(e8.cpu().numpy(), want[1]), axis
         assert int(cl.item()) == want[2], axis
+        G.release()
         del q, e8
     got = _dual_gpu(x, 1, rule, 0)
     assert np.array_equal(got[0], want_r[0]) and np.array_equal(got[1], want_r[1])
@@ -172,12 +187,11 @@ def test_mx_clip_boundaries(dtype):
             if rule == 0:
                 assert got[4] > 0 and got[5] > 0          # the thresholds are crossed
             for axis in (0, 1):
-                q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
-                e8 = torch.empty((rows, cols // 32) if axis == 0 else (rows // 32, cols), dtype=torch.uint8,
-                                 device="cuda")
-                cl = torch.empty(1, dtype=torch.int64, device="cuda")
+                q = G.empty((rows, cols), torch.uint8)
+                e8 = G.empty((rows, cols // 32) if axis == 0 else (rows // 32, cols), torch.uint8)
+                cl = G.empty(1, torch.int64)
                 F.mx_cast_ex(x, fmt, rule, 0, axis, q, e8, cl)
-                torch.cuda.synchronize()
+                G.check(f"fmt={fmt} rule={rule} axis={axis}")
                 q_o, e8_o, c_o = coracle.mx_cast_ex(xb, fmt, rule, 0, axis, 1)
                 assert np.array_equal(q.cpu().numpy(), q_o), (fmt, rule, axis)
                 assert np.array_equal(e8.cpu().numpy(), e8_o), (fmt, rule, axis)
@@ -190,17 +204,18 @@ def _ct_steps(shape, dtype, fmt, window, steps, make, estimator=F.EST_MAX_WINDOW
     o = policy.ScalingState(fmt, window, 1 if window else 0, 0, estimator, alpha, interval)
     for t in range(steps):
         x = make(t)
-        q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
-        qt = torch.empty(cols, rows, dtype=torch.uint8, device="cuda")
-        outs = torch.empty(2, dtype=torch.float32, device="cuda")
-        cl = torch.empty(1, dtype=torch.int64, device="cuda")
+        q = G.empty((rows, cols), torch.uint8)
+        qt = G.empty((cols, rows), torch.uint8)
+        outs = G.empty(2, torch.float32)
+        cl = G.empty(1, torch.int64)
         F.fp8q_cast_transpose(h, x, q, qt, outs[0:1], outs[1:2], cl)
-        torch.cuda.synchronize()
+        G.check(f"fp8q_cast_transpose {rows}x{cols} step {t}")
         q_o, a_o, s_o, c_o, _ = o.step(host_bits(x).reshape(-1), NT)
         q_o = q_o.reshape(rows, cols)
         assert np.array_equal(q.cpu().numpy(), q_o), t
         assert np.array_equal(qt.cpu().numpy(), q_o.T), t
         assert (f32bits(outs[0:1]), f32bits(outs[1:2]), int(cl.item())) == (s_o, a_o, c_o), t
+        G.release()
     assert F.fp8q_pipeline_status() == 0
     hist = F.fp8q_amax_history(h, max(1, window))
     assert [np.float32(v).view(np.uint32) for v in hist] == o.hist
@@ -234,10 +249,10 @@ def test_cast_transpose_edge_values(dtype, fmt):
                   lambda t, shape=shape: _edge_tensor(shape[0], shape[1], dtype, 100 * t + shape[1]) * (4.0 ** t))
 
 
-def _at(n, offset):
-    """A device byte buffer of n bytes starting `offset` bytes into a larger
-    allocation (allocations themselves are at least 256-byte aligned)."""
-    return torch.empty(n + 64, dtype=torch.uint8, device="cuda")[offset:offset + n]
+def _at(shape, offset):
+    """A guarded device byte buffer starting `offset` bytes past a 256-byte
+    boundary."""
+    return G.empty(shape, torch.uint8, offset=offset)
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
@@ -247,13 +262,13 @@ def test_mx_dual_offset_outputs(dtype):
     rows, cols = 160, 288
     x = _edge_tensor(rows, cols, dtype, 77)
     xb = host_bits(x)
-    qr = _at(rows * cols, 16).view(rows, cols)
-    er = _at(rows * cols // 32, 1).view(rows, cols // 32)
-    qc = _at(rows * cols, 48).view(cols, rows)
-    ec = _at(rows * cols // 32, 3).view(cols, rows // 32)
+    qr = _at((rows, cols), 16)
+    er = _at((rows, cols // 32), 1)
+    qc = _at((cols, rows), 48)
+    ec = _at((cols, rows // 32), 3)
     for fmt in (0, 1):
         F.mx_cast_dual(x, fmt, 0, 0, qr, er, qc, ec)
-        torch.cuda.synchronize()
+        G.check(f"fmt={fmt}")
         want = _dual_oracle(xb, fmt, 0, 0)
         for g, w in zip((qr, er, qc, ec), want[:4]):
             assert np.array_equal(g.cpu().numpy(), w), fmt
@@ -265,10 +280,10 @@ def test_cast_transpose_offset_outputs(dtype):
     x = _edge_tensor(rows, cols, dtype, 78)
     h = F.fp8q_create(0, 0)
     o = policy.ScalingState(0, 0)
-    q = _at(rows * cols, 16).view(rows, cols)
-    qt = _at(rows * cols, 48).view(cols, rows)
+    q = _at((rows, cols), 16)
+    qt = _at((cols, rows), 48)
     F.fp8q_cast_transpose(h, x, q, qt)
-    torch.cuda.synchronize()
+    G.check()
     q_o = o.step(host_bits(x).reshape(-1), NT)[0].reshape(rows, cols)
     assert np.array_equal(q.cpu().numpy(), q_o)
     assert np.array_equal(qt.cpu().numpy(), q_o.T)
@@ -278,8 +293,8 @@ def test_cast_transpose_offset_outputs(dtype):
 def test_cast_transpose_argument_checks():
     h = F.fp8q_create(0, 4)
     x = torch.zeros(48, 64, dtype=torch.bfloat16, device="cuda")
-    q = torch.empty(48, 64, dtype=torch.uint8, device="cuda")
-    qt = torch.empty(64, 48, dtype=torch.uint8, device="cuda")
+    q = G.empty((48, 64), torch.uint8)
+    qt = G.empty((64, 48), torch.uint8)
     with pytest.raises(F.Fp8qError) as ei:
         F.fp8q_cast_transpose(h, x, q, qt)             # rows not a multiple of 32
     assert ei.value.status == -1
@@ -330,11 +345,11 @@ def test_random_shapes_all_tiled_paths():
         cols16 = cols32 - 16 if cols32 > 32 and trial % 4 == 1 else cols32
         xc = x[:, :cols16].contiguous()
         xcb = host_bits(xc)
-        q = torch.empty(rows, cols16, dtype=torch.uint8, device="cuda")
-        e8 = torch.empty(rows // 32, cols16, dtype=torch.uint8, device="cuda")
-        cl = torch.empty(1, dtype=torch.int64, device="cuda")
+        q = G.empty((rows, cols16), torch.uint8)
+        e8 = G.empty((rows // 32, cols16), torch.uint8)
+        cl = G.empty(1, torch.int64)
         F.mx_cast_ex(xc, fmt, rule, 0, F.MX_COLWISE, q, e8, cl)
-        torch.cuda.synchronize()
+        G.check(f"trial {trial} column-wise")
         q_o, e8_o, c_o = coracle.mx_cast_ex(xcb, fmt, rule, 0, 1)
         assert np.array_equal(q.cpu().numpy(), q_o) and np.array_equal(e8.cpu().numpy(), e8_o), (trial, rows, cols16)
         assert int(cl.item()) == c_o, (trial, rows, cols16)

@@ -6,23 +6,31 @@ they run right after an out-of-memory error, or an allocation would stall a
 latency-bound loop.  fp8q_error_stats takes its per-CTA partial sums from
 cudaMallocAsync; the no-alloc variant takes them from a fixed array inside
 the library.  This file checks, through the C ABI, that the variant gives
-the same statistics as fp8q_error_stats (within the 1e-6 relative tolerance
-the other statistics tests use) on two different calls in a row -- the
-second smaller than the first, so rows left over from the first call must
-not leak into it -- and that it rejects a size beyond its limit.
+the statistics of the CPU oracle and of fp8q_error_stats -- MSE and bias
+within 1e-6 relative, the count exact -- on calls made in a row, each
+smaller than the one before, so partial sums left in the array by an
+earlier call must not leak into a later one; and that it rejects a size
+beyond its limit.
 
 Named to be collected last: a run that stops at the first failure has run
 every other test before this one.
 """
 import ctypes
+import os
 
+import numpy as np
 import pytest
 import torch
 
+from canary import Guards
+from oracle import coracle
 from tensor_scaling_cast_gb300 import fp8q as F
 from tensor_scaling_cast_gb300 import synthetic
 
 pytestmark = pytest.mark.gpu
+
+NT = os.cpu_count() or 1
+G = Guards(seed=0x20)
 
 
 @pytest.fixture(scope="module")
@@ -36,18 +44,22 @@ def lib():
 
 
 def _cast(x, fmt):
+    """A clipping per-tensor cast: the window holds a smaller tensor's amax."""
     g = F.ScaledCast(fmt, window=1)
-    g(x * 0.125)                                   # small window amax: the next cast clips
-    q, sinv, _, _ = g(x)
+    g(x * 0.125)
+    q, sinv, _, clipped = g(x)
+    torch.cuda.synchronize()
+    assert int(clipped.item()) > 0
     g.close()
     return q, sinv
 
 
-def _close(a, b):
-    mse, bias, n = a
-    mse_r, bias_r, n_r = b
-    return (n == n_r and abs(mse - mse_r) <= 1e-6 * mse_r
-            and abs(bias - bias_r) <= 1e-6 * max(abs(bias_r), mse_r ** 0.5))
+def _rel_close(a, b):
+    """Every statistic within 1e-6 relative of the reference (an exact zero
+    must be met exactly) and the counts equal."""
+    (mse, bias, n), (mse_r, bias_r, n_r) = a, b
+    return (int(n) == int(n_r) and abs(mse - mse_r) <= 1e-6 * abs(mse_r)
+            and abs(bias - bias_r) <= 1e-6 * abs(bias_r))
 
 
 def _noalloc(lib, x, q, fmt, sinv, out):
@@ -59,19 +71,35 @@ def _noalloc(lib, x, q, fmt, sinv, out):
                                         ctypes.c_void_p(out.data_ptr()), stream)
 
 
-def test_noalloc_stats_match_allocating_entry_point(lib):
+def _host_bits(x):
+    x = x.detach().contiguous().cpu()
+    if x.dtype == torch.bfloat16:
+        return x.view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    return x.view(torch.int32).numpy().view(np.uint32).reshape(-1)
+
+
+def test_noalloc_stats_match_oracle_and_allocating_entry_point(lib):
     cases = [
-        (synthetic.spike_step(9, "cuda", shape=(4096, 2048)), 0),    # 8 Mi elements: 8 rows
-        (synthetic.spike_step(3, "cuda", shape=(1000, 1000)).float(), 1),  # 1e6: 1 row
+        # 640 Mi + 12,345 bf16 elements: 641 slabs of 2^20, more CTAs than 4 per SM
+        (synthetic.mx_tanh("cuda", shape=((640 << 20) + 12345,), seed=4100), 0),
+        (synthetic.spike_step(9, "cuda", shape=(4096, 2048)), 1),          # 8 Mi: 4 CTAs per SM
+        (synthetic.spike_step(3, "cuda", shape=(1000, 1000)).float(), 0),  # fp32, 1e6 elements
     ]
-    for x, fmt in cases:                           # two calls in a row
+    for x, fmt in cases:                           # calls in a row, each smaller
         q, sinv = _cast(x, fmt)
         ref = torch.empty(3, dtype=torch.float64, device="cuda")
         F.fp8q_error_stats(x, q, fmt, sinv, ref)
-        out = torch.full((3,), float("nan"), dtype=torch.float64, device="cuda")
+        out = G.full(3, float("nan"), torch.float64)
         assert _noalloc(lib, x, q, fmt, sinv, out) == 0
-        torch.cuda.synchronize()
-        assert _close(out.cpu().tolist(), ref.cpu().tolist()), (out, ref)
+        G.check("after fp8q_error_stats_noalloc")
+        got = out.cpu().tolist()
+        e = -int(np.log2(sinv.item()))
+        want = coracle.stats(_host_bits(x), q.cpu().numpy().reshape(-1), fmt, e, NT)
+        assert _rel_close(got, want), (x.numel(), got, want)
+        assert _rel_close(got, ref.cpu().tolist()), (x.numel(), got, ref)
+        G.release()
+        del x, q, ref
+        torch.cuda.empty_cache()
 
 
 def test_noalloc_stats_rejects_size_above_limit(lib):
