@@ -13,6 +13,7 @@
 
 #include "fp8q.h"
 #include "fp8q_internal.cuh"
+#include "mx_device.cuh"
 
 namespace fp8q {
 
@@ -442,7 +443,7 @@ FP8Q_API int mx_cast_ex(const void* x, int dtype, int64_t rows, int64_t cols, in
   if (!dtype_ok(dtype) || !format_ok(format)) return FP8Q_EDTYPE;
   if (rule < FP8Q_MX_FLOOR || rule > FP8Q_MX_NEAREST) return FP8Q_EINVAL;
   if (axis != FP8Q_MX_ROWWISE && axis != FP8Q_MX_COLWISE) return FP8Q_EINVAL;
-  if (rows < 0 || cols <= 0 || headroom_bits < 0 || headroom_bits > 4) return FP8Q_EINVAL;
+  if (rows < 0 || cols <= 0 || headroom_bits < 0 || headroom_bits > kMaxHeadroom) return FP8Q_EINVAL;
   if (axis == FP8Q_MX_ROWWISE && cols % 32 != 0) return FP8Q_EINVAL;
   if (axis == FP8Q_MX_COLWISE && (rows % 32 != 0 || cols % 16 != 0)) return FP8Q_EINVAL;
   if (rows > 0 && cols > (int64_t(1) << 46) / rows) return FP8Q_EINVAL;
@@ -472,7 +473,7 @@ FP8Q_API int mx_cast_dual(const void* x, int dtype, int64_t rows, int64_t cols, 
   if (!dtype_ok(dtype) || !format_ok(format)) return FP8Q_EDTYPE;
   if (rule < FP8Q_MX_FLOOR || rule > FP8Q_MX_NEAREST) return FP8Q_EINVAL;
   if (rows < 0 || cols <= 0 || rows % 32 != 0 || cols % 32 != 0 || headroom_bits < 0 ||
-      headroom_bits > 4)
+      headroom_bits > kMaxHeadroom)
     return FP8Q_EINVAL;
   if (rows > 0 && cols > (int64_t(1) << 46) / rows) return FP8Q_EINVAL;
   if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return FP8Q_EINVAL;

@@ -70,9 +70,7 @@ __global__ void __launch_bounds__(kThreads, 4) mx_kernel(const char* __restrict_
         const float s = __uint_as_float((uint32_t)(127 - E) << 23);   // 2^-E
         out = cast_load<DT, FMT>(r[u], s);
         // per-element count only for blocks whose scaled max passes fmax
-        const int be = (int)(fmax_bits(FMT) >> 23) + E;
-        const uint32_t bound = be >= 255 ? 0x7F7FFFFFu : fmax_bits(FMT) + ((uint32_t)E << 23);
-        if (m > bound) {
+        if (mx_block_may_clip<FMT>(m, E)) {
 #pragma unroll
           for (int j = 0; j < EPL; ++j)
             lclip += clips<FMT>(__uint_as_float(elem_bits<DT>(r[u], j)) * s) ? 1u : 0u;

@@ -65,4 +65,20 @@ __device__ __forceinline__ int block_exp(uint32_t m, int rule, int headroom) {
   return min(127, max(-127, E + headroom));
 }
 
+// Finite bf16 / fp32 block maxima have k <= 127, so E <= 127 - emax_elem +
+// 1 (ceil) + headroom.  The casts scale by 2^-E as the normal fp32 number
+// with exponent field 127 - E, which needs E <= 126: headroom is therefore
+// capped (the C ABI rejects more than kMaxHeadroom).
+constexpr int kMaxHeadroom = 4;
+static_assert(127 - 8 + 1 + kMaxHeadroom <= 126, "2^-E must stay a normal fp32 number");
+
+// Can a finite block with max |x| bits m and shared exponent E hold a clipped
+// element?  Only if its scaled maximum m * 2^-E passes fmax, i.e. m exceeds
+// fmax * 2^E (never when that is beyond the fp32 range).
+template <int FMT>
+__device__ __forceinline__ bool mx_block_may_clip(uint32_t m, int E) {
+  const int be = (int)(fmax_bits(FMT) >> 23) + E;
+  return be < 255 && m > fmax_bits(FMT) + ((uint32_t)E << 23);
+}
+
 }  // namespace fp8q

@@ -158,8 +158,7 @@ __global__ void __launch_bounds__(kWThreads, FP8Q_TP_MINB) mx_dual_kernel(
 #pragma unroll
         for (int k = 0; k < NG; ++k) t[k] = cast_load<DT, FMT>(v[k], s);
         pack_row<DT, NG>(t, o);
-        const int be = (int)(fmax_bits(FMT) >> 23) + E;
-        if (C::kClipCount && be < 255 && m > fmax_bits(FMT) + ((uint32_t)E << 23)) {
+        if (C::kClipCount && mx_block_may_clip<FMT>(m, E)) {
 #pragma unroll
           for (int k = 0; k < 32; ++k)
             clip_r += clips<FMT>(__uint_as_float(elem_bits<DT>(v[k / EPL], k % EPL)) * s) ? 1u : 0u;

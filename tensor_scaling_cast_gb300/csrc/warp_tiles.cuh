@@ -185,8 +185,7 @@ __device__ __forceinline__ uint32_t mx_column(const uint32_t (&w)[32], uint32_t 
     ebyte = (uint32_t)(E + 127);
     const float s = __uint_as_float((uint32_t)(127 - E) << 23);
     cast32<FMT, HI>(w, s, o);
-    const int be = (int)(fmax_bits(FMT) >> 23) + E;
-    if (CNT && be < 255 && m > fmax_bits(FMT) + ((uint32_t)E << 23)) {
+    if (CNT && mx_block_may_clip<FMT>(m, E)) {
 #pragma unroll
       for (int k = 0; k < 32; ++k) clip += clips<FMT>(__uint_as_float(half_bits<HI>(w[k])) * s) ? 1u : 0u;
     }
