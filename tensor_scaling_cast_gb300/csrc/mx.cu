@@ -138,33 +138,14 @@ cudaError_t launch_mx(const void* x, int dtype, int64_t nelem, int format, int h
 // with byte permutes) that a TMA tiled store copies to q; the E8M0 bytes of a
 // sub-tile are one coalesced row segment.
 
-#ifndef FP8Q_COL_STAGES
-#define FP8Q_COL_STAGES 2
-#endif
-#ifndef FP8Q_COL_OBUF
-#define FP8Q_COL_OBUF 2
-#endif
-#ifndef FP8Q_COL_COLF
-#define FP8Q_COL_COLF true
-#endif
-#ifndef FP8Q_COL_L2PROMO
-#define FP8Q_COL_L2PROMO 128
-#endif
-#ifndef FP8Q_COL_MAXCTA
-#define FP8Q_COL_MAXCTA 0
-#endif
-#ifndef FP8Q_COL_CLIPFREE_STAGES
-#define FP8Q_COL_CLIPFREE_STAGES 3
-#endif
-#ifndef FP8Q_COL_CLIPFREE_MAXCTA
-#define FP8Q_COL_CLIPFREE_MAXCTA 2
-#endif
 // As many CTAs as fit when blocks may clip (the exact per-element count
-// needs the warps); two CTAs of three-stage warps per SM for a clip-free
-// cast (mx_clip_free), which is memory-bound.
-using ColCfg = TpCfg<FP8Q_COL_STAGES, FP8Q_COL_OBUF, 1, FP8Q_COL_COLF, 2048, FP8Q_COL_MAXCTA>;
-using ColClipFreeCfg =
-    TpCfg<FP8Q_COL_CLIPFREE_STAGES, FP8Q_COL_OBUF, 1, FP8Q_COL_COLF, 2048, FP8Q_COL_CLIPFREE_MAXCTA, false>;
+// needs the warps: four CTAs of two-stage warps per SM); two CTAs of
+// three-stage warps per SM for a clip-free cast (mx_clip_free), which is
+// memory-bound.  Column strips first; the L2 fetches 128 bytes per input
+// request.
+using ColCfg = TpCfg<2, 2, 1, true, 2048, 0>;
+using ColClipFreeCfg = TpCfg<3, 2, 1, true, 2048, 2, false>;
+constexpr int kColL2Promotion = 128;
 
 static __device__ unsigned int g_wait_timeouts;
 
@@ -251,7 +232,7 @@ static cudaError_t launch_mx_col_c(const void* x, int64_t rows, int64_t cols, in
   if (e != cudaSuccess) return e;
   if (C::kMaxCtasPerSm > 0 && occ > C::kMaxCtasPerSm) occ = C::kMaxCtasPerSm;
   CUtensorMap in, qm;
-  e = encode_tile_map(&in, x, DT == FP8Q_BF16, rows, cols, TILE_C, true, FP8Q_COL_L2PROMO);
+  e = encode_tile_map(&in, x, DT == FP8Q_BF16, rows, cols, TILE_C, true, kColL2Promotion);
   if (e == cudaSuccess) e = encode_byte_map(&qm, q, rows, cols, TILE_C, 32, TILE_C);
   if (e != cudaSuccess) return e;
   const long long need = ((rows / 32) * ctiles + kWWarps - 1) / kWWarps;

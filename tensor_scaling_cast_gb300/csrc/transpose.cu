@@ -33,61 +33,23 @@
 
 namespace fp8q {
 
-// Pipeline shape of each kernel (input stages per warp, output staging
-// buffers per warp, row tiles per chunk, CTAs per SM), overridable at build
-// time.  The cast + transpose moves little arithmetic per byte: it runs one
-// CTA of four warps per SM with six stages in flight per warp, which keeps
-// the read stream and its two write streams closer to the DRAM rate than
-// more, shallower warps do.  The MX dual carries much more arithmetic per
-// byte when its blocks clip (the exact per-element count) and needs the
-// warps; a clip-free MX dual (mx_clip_free) runs two CTAs per SM with three
-// stages per warp.
-#ifndef FP8Q_DUAL_STAGES
-#define FP8Q_DUAL_STAGES 2
-#endif
-#ifndef FP8Q_DUAL_OBUF
-#define FP8Q_DUAL_OBUF 2
-#endif
-#ifndef FP8Q_DUAL_CHUNK
-#define FP8Q_DUAL_CHUNK 4
-#endif
-#ifndef FP8Q_CT_STAGES
-#define FP8Q_CT_STAGES 6
-#endif
-#ifndef FP8Q_CT_OBUF
-#define FP8Q_CT_OBUF 1
-#endif
-#ifndef FP8Q_CT_MAXCTA
-#define FP8Q_CT_MAXCTA 1
-#endif
-#ifndef FP8Q_DUAL_MAXCTA
-#define FP8Q_DUAL_MAXCTA 0
-#endif
-#ifndef FP8Q_DUAL_CLIPFREE_STAGES
-#define FP8Q_DUAL_CLIPFREE_STAGES 3
-#endif
-#ifndef FP8Q_DUAL_CLIPFREE_MAXCTA
-#define FP8Q_DUAL_CLIPFREE_MAXCTA 2
-#endif
-#ifndef FP8Q_CT_CHUNK
-#define FP8Q_CT_CHUNK 4
-#endif
-#ifndef FP8Q_DUAL_COLF
-#define FP8Q_DUAL_COLF true
-#endif
-#ifndef FP8Q_CT_COLF
-#define FP8Q_CT_COLF true
-#endif
-#ifndef FP8Q_TP_L2PROMO
-#define FP8Q_TP_L2PROMO 128
-#endif
-#ifndef FP8Q_TP_MINB
-#define FP8Q_TP_MINB 4
-#endif
-using DualCfg = TpCfg<FP8Q_DUAL_STAGES, FP8Q_DUAL_OBUF, FP8Q_DUAL_CHUNK, FP8Q_DUAL_COLF, 4096, FP8Q_DUAL_MAXCTA>;
-using DualClipFreeCfg = TpCfg<FP8Q_DUAL_CLIPFREE_STAGES, FP8Q_DUAL_OBUF, FP8Q_DUAL_CHUNK, FP8Q_DUAL_COLF, 4096,
-                              FP8Q_DUAL_CLIPFREE_MAXCTA, false>;
-using CtCfg = TpCfg<FP8Q_CT_STAGES, FP8Q_CT_OBUF, FP8Q_CT_CHUNK, FP8Q_CT_COLF, 4096, FP8Q_CT_MAXCTA>;
+// Pipeline shape of each kernel: TpCfg<input stages per warp, output
+// staging buffers per warp, row tiles per chunk, column-strip-first chunk
+// order, staging bytes, CTAs per SM (0: as many as fit), clip count>.  The
+// cast + transpose moves little arithmetic per byte: it runs one CTA of four
+// warps per SM with six stages in flight per warp, which keeps the read
+// stream and its two write streams closer to the DRAM rate than more,
+// shallower warps do.  The MX dual carries much more arithmetic per byte
+// when its blocks may clip (the exact per-element count) and needs the warps
+// (three CTAs of two-stage warps per SM, the most shared memory allows); a
+// clip-free MX dual (mx_clip_free) runs two CTAs per SM with three stages per
+// warp.  Each shape was chosen by same-box measurement on bf16
+// [16384, 8192].
+using DualCfg = TpCfg<2, 2, 4, true, 4096, 0>;
+using DualClipFreeCfg = TpCfg<3, 2, 4, true, 4096, 2, false>;
+using CtCfg = TpCfg<6, 1, 4, true, 4096, 1>;
+constexpr int kTpL2Promotion = 128;      // bytes the L2 fetches per input-tile request
+constexpr int kTpMinBlocks = 4;          // launch bounds: at most 128 registers a thread
 
 static __device__ unsigned int g_tp_wait_timeouts;   // see fp8q_pipeline_status
 
@@ -103,7 +65,7 @@ cudaError_t read_tp_wait_timeouts(unsigned int* count) {
 // ---------------------------------------------------------------------------
 
 template <int DT, int FMT, class C>
-__global__ void __launch_bounds__(kWThreads, FP8Q_TP_MINB) mx_dual_kernel(
+__global__ void __launch_bounds__(kWThreads, kTpMinBlocks) mx_dual_kernel(
     const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
     const __grid_constant__ CUtensorMap qtmap, int64_t rows, int64_t cols, int rule, int headroom,
     uint8_t* __restrict__ e8_row, uint8_t* __restrict__ e8_colt, unsigned long long* clipped_row,
@@ -229,7 +191,7 @@ __global__ void __launch_bounds__(kWThreads, FP8Q_TP_MINB) mx_dual_kernel(
 // ---------------------------------------------------------------------------
 
 template <int DT, int FMT, class C>
-__global__ void __launch_bounds__(kWThreads, FP8Q_TP_MINB) cast_transpose_kernel(
+__global__ void __launch_bounds__(kWThreads, kTpMinBlocks) cast_transpose_kernel(
     const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
     const __grid_constant__ CUtensorMap qtmap, int64_t rows, int64_t cols, DevState* st, int mode,
     GroupHeader h) {
@@ -390,7 +352,7 @@ template <int DT>
 static cudaError_t tp_maps(const void* x, int64_t rows, int64_t cols, uint8_t* q, uint8_t* qt, CUtensorMap* in,
                            CUtensorMap* qmap, CUtensorMap* qtmap) {
   constexpr int TILE_C = TileGeom<DT>::TILE_C;
-  cudaError_t e = encode_tile_map(in, x, DT == FP8Q_BF16, rows, cols, TILE_C, true, FP8Q_TP_L2PROMO);
+  cudaError_t e = encode_tile_map(in, x, DT == FP8Q_BF16, rows, cols, TILE_C, true, kTpL2Promotion);
   if (e == cudaSuccess) e = encode_byte_map(qmap, q, rows, cols, TILE_C, 32, TILE_C);
   if (e == cudaSuccess) e = encode_byte_map(qtmap, qt, cols, rows, 32, TILE_C, 32);
   return e;
