@@ -103,8 +103,12 @@ def test_mx_dual_full_size(rule):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_mx_dual_edge_values(dtype):
     """Zero / NaN / Inf / subnormal / huge blocks, ragged column tiles,
-    both formats, every rule, headroom 0 and 2."""
-    for rows, cols in ((96, 320), (32, 32), (64, 288), (160, 96)):
+    both formats, every rule, headroom 0 and 2.  Widths of 256 and 512
+    columns give column-tile counts divisible by the warps of a CTA, so the
+    row-block scale bytes go through the CTA's pooled table (with a ragged
+    last row chunk at 96 and 160 rows); the other widths store them from
+    each warp."""
+    for rows, cols in ((96, 320), (32, 32), (64, 288), (160, 96), (96, 256), (160, 512)):
         x = _edge_tensor(rows, cols, dtype, rows * 7 + cols)
         xb = host_bits(x)
         for fmt in (0, 1):
