@@ -138,24 +138,24 @@ cudaError_t launch_mx(const void* x, int dtype, int64_t nelem, int format, int h
 // with byte permutes) that a TMA tiled store copies to q; the E8M0 bytes of a
 // sub-tile are one coalesced row segment.
 
-// As many CTAs as fit when blocks may clip (the exact per-element count
-// needs the warps: four CTAs of two-stage warps per SM); two CTAs of
-// three-stage warps per SM for a clip-free cast (mx_clip_free), which is
-// memory-bound.  Column strips first; the L2 fetches 128 bytes per input
-// request.
-using ColCfg = TpCfg<2, 2, 1, true, 2048, 0>;
+// Sixteen two-stage warps per SM, in one CTA (adjacent column tiles), when
+// blocks may clip (the exact per-element count needs the warps); two CTAs
+// of four three-stage warps per SM for a clip-free cast (mx_clip_free),
+// which is memory-bound.  Column strips first; the L2 fetches 128 bytes per
+// input request.
+using ColCfg = TpCfg<2, 2, 1, true, 2048, 1, true, 16>;
 using ColClipFreeCfg = TpCfg<3, 2, 1, true, 2048, 2, false>;
 constexpr int kColL2Promotion = 128;
 
 static __device__ unsigned int g_wait_timeouts;
 
 template <int DT, int FMT, class C>
-__global__ void __launch_bounds__(kWThreads, 4) mx_colwise_kernel(
+__global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) mx_colwise_kernel(
     const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap, int64_t rows,
     int64_t cols, uint8_t* __restrict__ e8m0, unsigned long long* clipped, int headroom, int rule) {
   constexpr int TILE_C = TileGeom<DT>::TILE_C;
   extern __shared__ __align__(1024) uint4 dyn_smem[];
-  __shared__ __align__(8) uint64_t full[kWWarps][C::kStages];
+  __shared__ __align__(8) uint64_t full[C::kWarps][C::kStages];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t ctiles = (uint32_t)((cols + TILE_C - 1) / TILE_C);
   uint8_t* region = warp_region<C>(dyn_smem, warp);
@@ -228,18 +228,18 @@ static cudaError_t launch_mx_col_c(const void* x, int64_t rows, int64_t cols, in
   const int64_t ctiles = (cols + TILE_C - 1) / TILE_C;
   if ((rows / 32) * ctiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // 32-bit tile counts
   int occ = 1;
-  cudaError_t e = kernel_occupancy(reinterpret_cast<const void*>(kern), kWThreads, C::kSmemBytes, &occ);
+  cudaError_t e = kernel_occupancy(reinterpret_cast<const void*>(kern), C::kThreads, C::kSmemBytes, &occ);
   if (e != cudaSuccess) return e;
   if (C::kMaxCtasPerSm > 0 && occ > C::kMaxCtasPerSm) occ = C::kMaxCtasPerSm;
   CUtensorMap in, qm;
   e = encode_tile_map(&in, x, DT == FP8Q_BF16, rows, cols, TILE_C, true, kColL2Promotion);
   if (e == cudaSuccess) e = encode_byte_map(&qm, q, rows, cols, TILE_C, 32, TILE_C);
   if (e != cudaSuccess) return e;
-  const long long need = ((rows / 32) * ctiles + kWWarps - 1) / kWWarps;
+  const long long need = ((rows / 32) * ctiles + C::kWarps - 1) / C::kWarps;
   long long grid = (long long)sm_count(device_of_current()) * occ;
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, kWThreads, C::kSmemBytes, s>>>(in, qm, rows, cols, e8m0, clipped, headroom, rule);
+  kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, s>>>(in, qm, rows, cols, e8m0, clipped, headroom, rule);
   ++*launches;
   return cudaGetLastError();
 }

@@ -35,21 +35,22 @@ namespace fp8q {
 
 // Pipeline shape of each kernel: TpCfg<input stages per warp, output
 // staging buffers per warp, row tiles per chunk, column-strip-first chunk
-// order, staging bytes, CTAs per SM (0: as many as fit), clip count>.  The
-// cast + transpose moves little arithmetic per byte: it runs one CTA of four
-// warps per SM with six stages in flight per warp, which keeps the read
-// stream and its two write streams closer to the DRAM rate than more,
-// shallower warps do.  The MX dual carries much more arithmetic per byte
-// when its blocks may clip (the exact per-element count) and needs the warps
-// (three CTAs of two-stage warps per SM, the most shared memory allows); a
-// clip-free MX dual (mx_clip_free) runs two CTAs per SM with three stages per
-// warp.  Each shape was chosen by same-box measurement on bf16
+// order, staging bytes, CTAs per SM (0: as many as fit), clip count, warps
+// per CTA>.  The cast + transpose moves little arithmetic per byte: it runs
+// one CTA of four warps per SM with six stages in flight per warp, which
+// keeps the read stream and its two write streams closer to the DRAM rate
+// than more, shallower warps do.  The MX dual carries much more arithmetic
+// per byte when its blocks may clip (the exact per-element count) and needs
+// the warps: twelve two-stage warps per SM, the most shared memory allows,
+// all in one CTA so that they work on twelve adjacent column tiles (a CTA's
+// warps on distant chunks cost 5%); a clip-free MX dual (mx_clip_free) runs
+// two CTAs of four three-stage warps per SM (one CTA of eight measured 2.8%
+// slower there).  Each shape was chosen by same-box measurement on bf16
 // [16384, 8192].
-using DualCfg = TpCfg<2, 2, 4, true, 4096, 0>;
+using DualCfg = TpCfg<2, 2, 4, true, 4096, 1, true, 12>;
 using DualClipFreeCfg = TpCfg<3, 2, 4, true, 4096, 2, false>;
 using CtCfg = TpCfg<6, 1, 4, true, 4096, 1>;
 constexpr int kTpL2Promotion = 128;      // bytes the L2 fetches per input-tile request
-constexpr int kTpMinBlocks = 4;          // launch bounds: at most 128 registers a thread
 
 static __device__ unsigned int g_tp_wait_timeouts;   // see fp8q_pipeline_status
 
@@ -65,7 +66,7 @@ cudaError_t read_tp_wait_timeouts(unsigned int* count) {
 // ---------------------------------------------------------------------------
 
 template <int DT, int FMT, class C>
-__global__ void __launch_bounds__(kWThreads, kTpMinBlocks) mx_dual_kernel(
+__global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) mx_dual_kernel(
     const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
     const __grid_constant__ CUtensorMap qtmap, int64_t rows, int64_t cols, int rule, int headroom,
     uint8_t* __restrict__ e8_row, uint8_t* __restrict__ e8_colt, unsigned long long* clipped_row,
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(kWThreads, kTpMinBlocks) mx_dual_kernel(
   constexpr int EPL = G::EPL, TILE_C = G::TILE_C, NG = G::NG;
   constexpr int QROWB = TILE_C;                      // bytes per row of the row-major part
   extern __shared__ __align__(1024) uint4 dyn_smem[];
-  __shared__ __align__(8) uint64_t full[kWWarps][C::kStages];
+  __shared__ __align__(8) uint64_t full[C::kWarps][C::kStages];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t ctiles = (uint32_t)((cols + TILE_C - 1) / TILE_C);
   uint8_t* region = warp_region<C>(dyn_smem, warp);
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(kWThreads, kTpMinBlocks) mx_dual_kernel(
 // ---------------------------------------------------------------------------
 
 template <int DT, int FMT, class C>
-__global__ void __launch_bounds__(kWThreads, kTpMinBlocks) cast_transpose_kernel(
+__global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) cast_transpose_kernel(
     const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
     const __grid_constant__ CUtensorMap qtmap, int64_t rows, int64_t cols, DevState* st, int mode,
     GroupHeader h) {
@@ -199,9 +200,9 @@ __global__ void __launch_bounds__(kWThreads, kTpMinBlocks) cast_transpose_kernel
   constexpr int TILE_C = G::TILE_C, NG = G::NG;
   constexpr int QROWB = TILE_C;
   extern __shared__ __align__(1024) uint4 dyn_smem[];
-  __shared__ __align__(8) uint64_t full[kWWarps][C::kStages];
+  __shared__ __align__(8) uint64_t full[C::kWarps][C::kStages];
   __shared__ int s_e;
-  __shared__ uint32_t s_nonfin[kWWarps];
+  __shared__ uint32_t s_nonfin[C::kWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t ctiles = (uint32_t)((cols + TILE_C - 1) / TILE_C);
   const uint32_t ntiles = (uint32_t)(rows / 32) * ctiles;
@@ -336,11 +337,11 @@ static cudaError_t tp_grid(const void* kern, int64_t rows, int64_t cols, long lo
   if ((rows / 32) * ctiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // 32-bit tile counts
   const int64_t nchunks = ((rows / 32 + C::kChunk - 1) / C::kChunk) * ctiles;
   int occ = 1;
-  cudaError_t e = kernel_occupancy(kern, kWThreads, C::kSmemBytes, &occ);
+  cudaError_t e = kernel_occupancy(kern, C::kThreads, C::kSmemBytes, &occ);
   if (e != cudaSuccess) return e;
   if (C::kMaxCtasPerSm > 0 && occ > C::kMaxCtasPerSm) occ = C::kMaxCtasPerSm;
   long long gr = (long long)sm_count(device_of_current()) * occ;
-  const long long need = (nchunks + kWWarps - 1) / kWWarps;
+  const long long need = (nchunks + C::kWarps - 1) / C::kWarps;
   if (gr > need) gr = need;
   *grid = gr < 1 ? 1 : gr;
   return cudaSuccess;
@@ -370,7 +371,7 @@ static cudaError_t launch_dual_c(const void* x, int64_t rows, int64_t cols, int 
   CUtensorMap in, qm, qtm;
   e = tp_maps<DT>(x, rows, cols, q_row, q_colt, &in, &qm, &qtm);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)grid, kWThreads, C::kSmemBytes, s>>>(in, qm, qtm, rows, cols, rule, headroom, e8_row, e8_colt,
+  kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, s>>>(in, qm, qtm, rows, cols, rule, headroom, e8_row, e8_colt,
                                                         cr, cc);
   ++*launches;
   return cudaGetLastError();
@@ -412,7 +413,7 @@ static cudaError_t launch_ct_t(const void* x, int64_t rows, int64_t cols, uint8_
   CUtensorMap in, qm, qtm;
   e = tp_maps<DT>(x, rows, cols, q, qt, &in, &qm, &qtm);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)grid, kWThreads, CtCfg::kSmemBytes, s>>>(in, qm, qtm, rows, cols, st, mode, h);
+  kern<<<(unsigned)grid, CtCfg::kThreads, CtCfg::kSmemBytes, s>>>(in, qm, qtm, rows, cols, st, mode, h);
   ++*launches;
   return cudaGetLastError();
 }

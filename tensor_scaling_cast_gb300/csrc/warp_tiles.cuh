@@ -25,28 +25,34 @@
 
 namespace fp8q {
 
-constexpr int kWWarps = 4;                             // warps per CTA
-constexpr int kWThreads = 32 * kWWarps;
 constexpr int kWTileBytes = 32 * 128;                  // 32 rows x 128 bytes
 constexpr int kWTileVec = kWTileBytes / 16;            // uint4 per sub-tile
 
 // Pipeline shape of one kernel: S input stages per warp, OB output staging
 // buffers of OUTB bytes per warp, CH row tiles per chunk, chunk order, at
-// most MAXC resident CTAs per SM (0: as many as fit), and whether the MX
-// kernels count clipped elements (CNT false only for clip-free casts, which
-// cannot clip).
-template <int S, int OB, int CH, bool COLF, int OUTB, int MAXC = 0, bool CNT = true>
+// most MAXC resident CTAs per SM (0: as many as fit), whether the MX kernels
+// count clipped elements (CNT false only for clip-free casts, which cannot
+// clip), and W warps per CTA.  A CTA's warps start on W consecutive chunks
+// and advance together by the grid's warp count, so with column strips
+// first they always hold W adjacent column tiles of one row band: an SM
+// whose warps all sit in one CTA reads and writes one wide band at a time.
+template <int S, int OB, int CH, bool COLF, int OUTB, int MAXC = 0, bool CNT = true, int W = 4>
 struct TpCfg {
   static_assert(S >= 2 && S <= 8, "input stages");
   static_assert(OB == 1 || OB == 2, "one or two output staging buffers");
   static_assert(CH >= 1 && CH <= 8, "the column E8M0 run is kept in one 64-bit word");
   static_assert(OUTB % 1024 == 0, "staging buffers keep the 1024-byte alignment of the swizzle");
+  static_assert(W >= 1 && W <= 16, "warps per CTA");
   static constexpr int kStages = S, kOutBufs = OB, kChunk = CH, kOutBytes = OUTB;
   static constexpr bool kColFastest = COLF;      // chunk order: column tile fastest
   static constexpr int kMaxCtasPerSm = MAXC;
   static constexpr bool kClipCount = CNT;
+  static constexpr int kWarps = W, kThreads = 32 * W;
+  // launch bounds: CTAs per SM the register budget must allow (at most 128
+  // registers a thread, fewer CTAs for wider ones)
+  static constexpr int kMinBlocks = W >= 16 ? 1 : 16 / W;
   static constexpr int kWarpBytes = S * kWTileBytes + OB * OUTB;
-  static constexpr int kSmemBytes = kWWarps * kWarpBytes + 1024;   // + alignment slack
+  static constexpr int kSmemBytes = W * kWarpBytes + 1024;   // + alignment slack
 };
 
 // True when no block of an MX cast can clip: under the round-up rule the
@@ -254,10 +260,10 @@ struct WarpPipe {
     const uint32_t rchunks = (row_tiles + kChunkR - 1) / kChunkR;
     nchunks = rchunks * col_tiles;
     nfast = kColF ? col_tiles : rchunks;
-    stride = gridDim.x * kWWarps;
+    stride = gridDim.x * C::kWarps;
     sq = stride / nfast;
     sr = stride % nfast;
-    cur.v = blockIdx.x * kWWarps + (threadIdx.x >> 5);
+    cur.v = blockIdx.x * C::kWarps + (threadIdx.x >> 5);
     cur.sl = cur.v / nfast;
     cur.fa = cur.v % nfast;
     cur.i = 0;
