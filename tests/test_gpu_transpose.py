@@ -360,3 +360,35 @@ def test_random_shapes_all_tiled_paths():
         # per-tensor cast + transpose, current scaling then a delayed step
         _ct_steps((rows, cols32), dtype, fmt, 2, 2, lambda t, x=x: x * (2.0 ** (3 * t)))
     assert F.fp8q_pipeline_status() == 0
+
+
+@pytest.mark.parametrize("dtype,shape", [(torch.bfloat16, (16416, 4160)), (torch.float32, (8224, 1056))])
+def test_large_ragged_shapes(dtype, shape):
+    """Shapes that give every warp of a full grid several chunks, with a
+    ragged last row chunk (rows / 32 odd) and, for fp32, a ragged last
+    column chunk band: the MX dual, the column-wise MX cast and the
+    per-tensor cast + transpose, byte for byte, twice in a row."""
+    rows, cols = shape
+    rng = np.random.default_rng(rows + cols)
+    x = torch.from_numpy((rng.standard_normal(shape) * np.exp(rng.uniform(-6, 6, size=(rows, 1))))
+                         .astype(np.float32)).to(dtype).cuda()
+    xb = host_bits(x)
+    for rule in (0, 1):
+        want = _dual_oracle(xb, 0, rule, 0, NT)
+        for _ in range(2):
+            got = _dual_gpu(x, 0, rule, 0)
+            for g, w, nm in zip(got[:4], want[:4], ["q_row", "e8m0_row", "q_colt", "e8m0_colt"]):
+                assert np.array_equal(g, w), (shape, rule, nm)
+            assert got[4:] == list(want[4:]), (shape, rule)
+        q_o, e8_o, c_o = coracle.mx_cast_ex(xb, 0, rule, 0, 1, NT)
+        for _ in range(2):
+            q = G.empty((rows, cols), torch.uint8)
+            e8 = G.empty((rows // 32, cols), torch.uint8)
+            cl = G.empty(1, torch.int64)
+            F.mx_cast_ex(x, 0, rule, 0, 1, q, e8, cl)
+            G.check("column-wise")
+            assert np.array_equal(q.cpu().numpy(), q_o) and np.array_equal(e8.cpu().numpy(), e8_o), (shape, rule)
+            assert int(cl.item()) == c_o
+            G.release()
+    _ct_steps(shape, dtype, 0, 4, 3, lambda t: x * (2.0 ** t))
+    assert F.fp8q_pipeline_status() == 0
