@@ -41,13 +41,14 @@ namespace fp8q {
 // keeps the read stream and its two write streams closer to the DRAM rate
 // than more, shallower warps do.  The MX dual carries much more arithmetic
 // per byte when its blocks may clip (the exact per-element count) and needs
-// the warps: twelve two-stage warps per SM, the most shared memory allows,
-// all in one CTA so that they work on twelve adjacent column tiles (a CTA's
-// warps on distant chunks cost 5%); a clip-free MX dual (mx_clip_free) runs
-// two CTAs of four three-stage warps per SM (one CTA of eight measured 2.8%
-// slower there).  Each shape was chosen by same-box measurement on bf16
-// [16384, 8192].
-using DualCfg = TpCfg<2, 2, 4, true, 4096, 1, true, 12>;
+// the warps: twelve warps per SM (ten or fourteen measured slower), each
+// with three input stages and one staging buffer, which is what shared
+// memory allows, all in one CTA so that they work on twelve adjacent column
+// tiles (a CTA's warps on distant chunks cost 5%); a clip-free MX dual
+// (mx_clip_free) runs two CTAs of four three-stage warps per SM (one CTA of
+// eight measured 2.8% slower there).  Each shape was chosen by same-box
+// measurement on bf16 [16384, 8192].
+using DualCfg = TpCfg<3, 1, 4, true, 4096, 1, true, 12>;
 using DualClipFreeCfg = TpCfg<3, 2, 4, true, 4096, 2, false>;
 using CtCfg = TpCfg<6, 1, 4, true, 4096, 1>;
 constexpr int kTpL2Promotion = 128;      // bytes the L2 fetches per input-tile request
