@@ -102,7 +102,10 @@ typedef struct fp8q_state* fp8q_handle;
  *   margin_bits >= 0 and <= 16: the scale keeps amax <= fmax / 2^margin
  *   hysteresis_bits >= 0 and <= 16 (0 = off)
  * Allocates the state in device memory of the current device (cudaMalloc).
- * *out receives the handle; FP8Q_ENOMEM / FP8Q_ECUDA on failure. */
+ * *out receives the handle; FP8Q_ENOMEM / FP8Q_ECUDA on failure.  The state
+ * lives in the device's current context: once that context is destroyed
+ * (cudaDeviceReset), destroy the handle and create a new one -- the old
+ * handle's device state no longer exists. */
 FP8Q_API int fp8q_create(int format, int window, int margin_bits, int hysteresis_bits,
                          fp8q_handle* out);
 

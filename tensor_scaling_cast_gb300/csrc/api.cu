@@ -1,5 +1,7 @@
 // C ABI of libfp8q: argument checks, handle lifecycle, launch planning.
 // Every entry point returns a status; nothing throws across the ABI.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -35,18 +37,44 @@ int device_of_current() {
   return d;
 }
 
+// Id of the calling thread's current CUDA context (0 if none or unknown):
+// what a device-resident address or a per-function attribute is valid for.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  unsigned long long id = 0;
+  return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
+
 // Resident CTAs per SM of a kernel at `threads` threads and `smem` bytes of
-// dynamic shared memory, computed once per (kernel, size, device); the
-// kernel's dynamic shared-memory limit is raised to `smem` first when that
-// exceeds the 48 KiB default.  Thread-safe.
+// dynamic shared memory, computed once per (kernel, size, device, context);
+// the kernel's dynamic shared-memory limit is raised to `smem` first when
+// that exceeds the 48 KiB default (an attribute of the context, so a
+// re-created context sets it again).  Thread-safe.
 cudaError_t kernel_occupancy(const void* kernel, int threads, int smem, int* occ) {
-  struct Entry { const void* k; int threads, smem, device, occ; };
+  struct Entry { const void* k; int threads, smem, device; unsigned long long ctx; int occ; };
   static std::mutex mu;
   static std::vector<Entry> cache;
   const int device = device_of_current();
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lk(mu);
   for (const Entry& en : cache)
-    if (en.k == kernel && en.threads == threads && en.smem == smem && en.device == device) {
+    if (en.k == kernel && en.threads == threads && en.smem == smem && en.device == device && ctx != 0 &&
+        en.ctx == ctx) {
       *occ = en.occ;
       return cudaSuccess;
     }
@@ -57,7 +85,7 @@ cudaError_t kernel_occupancy(const void* kernel, int threads, int smem, int* occ
   int v = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, threads, (size_t)smem) != cudaSuccess || v < 1)
     v = 1;
-  cache.push_back({kernel, threads, smem, device, v});
+  cache.push_back({kernel, threads, smem, device, ctx, v});
   *occ = v;
   return cudaSuccess;
 }

@@ -171,26 +171,7 @@ struct ScratchEntry {
 static std::mutex g_scratch_mu;
 static ScratchEntry g_scratch[128] = {};
 
-static unsigned long long current_context_id() {
-  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
-  static PFN_cuCtxGetId_v12000 get_id = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult qr;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &qr) == cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
-  });
-  if (!get_current || !get_id) return 0;
-  CUcontext c = nullptr;
-  if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
-  unsigned long long id = 0;
-  return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
-}
+unsigned long long current_context_id();   // api.cu
 
 static cudaError_t stats_scratch(int device, double** out) {
   if (device < 0 || device >= 128) return cudaErrorInvalidDevice;
