@@ -176,7 +176,20 @@ FP8Q_API int fp8q_cast(fp8q_handle h, const void* x, int dtype, int64_t n, uint8
  * pointers); the handles must be distinct.  d_scale_inv, d_amax, d_clipped
  * are DEVICE arrays of length count (or NULL).  Work is split into equal
  * 32 KiB input chunks over all tensors; each tensor keeps its own state.
- * count > 0; groups above 512 tensors are split into several launches. */
+ * count > 0; groups above 512 tensors are split into several launches.
+ *
+ * CUDA graphs (stream capture), for fp8q_cast, fp8q_cast_multi(_ex),
+ * fp8q_cast_transpose and fp8q_loss_scaler_update: a cast may be captured
+ * once each of its handles has done its first cast, or has window 0 under
+ * the max-window estimator.  A handle's first cast under a window or the
+ * smoothed estimator takes the current-scaling path, chosen on the host, so
+ * while its stream captures it returns FP8Q_EINVAL and captures nothing.
+ * Every launch of the graph advances the handles' device state exactly as
+ * the same eager calls would.  A captured call does not mark its handle:
+ * synchronise the stream the graph runs on before reading or setting the
+ * handle's state (fp8q_amax_history, fp8q_scale_state, fp8q_set_history,
+ * fp8q_reset, the estimator state, fp8q_loss_scaler_read), which are host
+ * calls and not capturable themselves. */
 FP8Q_API int fp8q_cast_multi(const fp8q_handle* hs, const void* const* xs, const int* dtypes,
                              const int64_t* ns, uint8_t* const* qs, float* d_scale_inv,
                              float* d_amax, unsigned long long* d_clipped, int count,

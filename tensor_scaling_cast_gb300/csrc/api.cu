@@ -141,7 +141,29 @@ static int wait_last(fp8q_handle h) {
   return e == cudaSuccess ? FP8Q_OK : fail_cuda(e);
 }
 
+// Is s capturing into a CUDA graph?
+static bool stream_capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return cs == cudaStreamCaptureStatusActive;
+}
+
+// Would the handle's next cast be its first one under an estimator that
+// takes current scaling only then (window > 0, or the smoothed average)?
+// Such a cast picks its path on the host from that fact, so it must not be
+// captured into a graph whose replays come later.
+static bool first_windowed_cast(fp8q_handle h) {
+  return h->estimator == FP8Q_EST_SMOOTHED ? h->host_casts == 0 : (h->window > 0 && h->host_count == 0);
+}
+
+// After a cast enqueued on s: remember it for the host reads of the state.
+// A cast captured into a graph is not recorded (its replays are the
+// caller's to wait for).
 static int record_last(fp8q_handle h, cudaStream_t s) {
+  if (stream_capturing(s)) return FP8Q_OK;
   cudaError_t e = cudaEventRecord(h->last, s);
   if (e != cudaSuccess) return fail_cuda(e);
   h->has_last = true;
@@ -262,6 +284,9 @@ static int plan_and_launch(const fp8q_handle* hs, const void* const* xs, const i
                            float* d_amax, unsigned long long* d_clipped,
                            unsigned long long* d_nonfinite, unsigned long long* d_underflow,
                            int count, cudaStream_t s) {
+  if (stream_capturing(s))
+    for (int i = 0; i < count; ++i)
+      if (first_windowed_cast(hs[i])) return FP8Q_EINVAL;
   for (int base = 0; base < count; base += kMaxGroup) {
     const int m = std::min(kMaxGroup, count - base);
     std::vector<TensorDesc> all(m), pre;
@@ -443,6 +468,7 @@ FP8Q_API int fp8q_loss_scaler_update(fp8q_loss_scaler ls, const unsigned long lo
   e = launch_loss_scale_update(ls->dev, d_nonfinite, count, d_scale, d_skip, s, &launches);
   g_launches += launches;
   if (e != cudaSuccess) return fail_cuda(e);
+  if (stream_capturing(s)) return FP8Q_OK;      // a captured update: the replays are the caller's to wait for
   e = cudaEventRecord(ls->last, s);
   if (e != cudaSuccess) return fail_cuda(e);
   ls->has_last = true;
@@ -536,6 +562,7 @@ FP8Q_API int fp8q_cast_transpose(fp8q_handle h, const void* x, int dtype, int64_
   int st = check_device(h);
   if (st != FP8Q_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (stream_capturing(s) && first_windowed_cast(h)) return FP8Q_EINVAL;
   const int64_t n = rows * cols;
   const bool current = h->estimator == FP8Q_EST_SMOOTHED ? h->host_casts == 0
                                                          : (h->window == 0 || h->host_count == 0);
