@@ -52,7 +52,9 @@
  *    elements; q receives n bytes in the same order.
  *  - A handle belongs to the device that was current at fp8q_create and must
  *    be used with that device current (else FP8Q_EDEVICE).  A handle keeps
- *    state across calls: do not use one handle from two streams at once.
+ *    state across calls: do not use one handle from two streams or two host
+ *    threads at once.  Distinct handles are independent: casts on different
+ *    handles may run on different streams and host threads concurrently.
  *  - The library has no CPU path: without a usable GPU every compute call
  *    returns FP8Q_ECUDA.
  */

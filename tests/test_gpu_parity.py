@@ -204,6 +204,44 @@ def run_group_steps(fmts, windows, xs_steps, margin=0, hyst=0, names=None):
         F.fp8q_destroy(h)
 
 
+def test_two_streams_with_distinct_handles():
+    """Two groups of handles cast on two streams with no ordering between
+    them, four steps each (the launches may overlap on the GPU): every byte,
+    amax, scale_inv and clipped count of both groups equal the oracle's."""
+    specs = synthetic.decoder_tensor_specs(layers=1, hidden=256, ffn=1024, tokens=512)
+    groups = [specs[0::2], specs[1::2]]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    hs = [[F.fp8q_create(sp[2], 4, 0, 0) for sp in grp] for grp in groups]
+    orc = [[policy.ScalingState(sp[2], 4, 0, 0) for sp in grp] for grp in groups]
+    for t in range(4):
+        xs = [[synthetic.decoder_tensor(sp, t, "cuda") for sp in grp] for grp in groups]
+        torch.cuda.synchronize()
+        outs = []
+        for gi, st in enumerate(streams):
+            n = len(groups[gi])
+            qs = [G.empty(x.numel(), torch.uint8) for x in xs[gi]]
+            o = (G.empty(n, torch.float32), G.empty(n, torch.float32), G.empty(n, torch.int64))
+            torch.cuda.synchronize()             # the guard fills are done before either stream starts
+            outs.append((qs, o))
+        for gi, st in enumerate(streams):
+            qs, o = outs[gi]
+            F.fp8q_cast_multi(hs[gi], xs[gi], qs, *o, stream=st)
+        torch.cuda.synchronize()
+        G.check(f"step {t}")
+        for gi in range(2):
+            qs, (sinv, amax, clipped) = outs[gi]
+            sb, ab, cb = f32bits(sinv), f32bits(amax), clipped.cpu().numpy()
+            for i, x in enumerate(xs[gi]):
+                q_o, a_o, s_o, c_o, _ = orc[gi][i].step(host_bits(x), NT)
+                assert np.array_equal(qs[i].cpu().numpy(), q_o.reshape(-1)), (t, gi, i)
+                assert ab[i] == a_o and sb[i] == s_o and int(cb[i]) == c_o, (t, gi, i)
+        G.release()
+    for gi in range(2):
+        for h, o in zip(hs[gi], orc[gi]):
+            assert F.fp8q_scale_state(h) == (o.prev_e, o.steps)
+            F.fp8q_destroy(h)
+
+
 def test_grad_group_reduced_sizes():
     """64 gradient-like bf16 tensors (sides 64..512) -> E5M2, window 16, one
     grouped launch per step, 4 steps (step 0 is current scaling)."""
