@@ -22,6 +22,10 @@ Besides the timed figures, each line carries `results` (what the
 configurations ask to report, computed with the library outside the timed
 region) and `inputs_sha256` (the SHA-256 of every input tensor's bytes), so
 the reported fractions can be tied to the exact inputs that produced them.
+Workloads of several parts also carry `parts_after_clean_l2`: each part
+timed alone after a read of 1 GiB that leaves no dirty line in L2, i.e.
+without the write-back of the previous part's output that a part absorbs
+inside a step (`parts`).
 """
 from __future__ import annotations
 
@@ -562,6 +566,8 @@ def run_ours(args, rank: int, world: int):
     dpart = parts[dom.name]
 
     copy_ref = copy_reference(dev, W.step_bytes)
+    clean = (parts_after_clean_l2(W, dev, min(K, 10), warm + K, peak)
+             if len(W.parts) > 1 and not W.graph_steps else None)
     results = workload_results(args.workload, dev) if rank == 0 else None
     digests = input_digests(W) if rank == 0 else None
     e2e = None
@@ -625,6 +631,8 @@ def run_ours(args, rank: int, world: int):
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        if clean is not None:
+            line["parts_after_clean_l2"] = clean
         if args.workload == "current":
             line["latency_us_per_cast"] = round(ms_step * 1e3, 2)
         if results is not None:
@@ -632,6 +640,34 @@ def run_ours(args, rank: int, world: int):
         if digests is not None:
             line["inputs_sha256"] = digests
         print(json.dumps(line), flush=True)
+
+
+def parts_after_clean_l2(W, dev, steps: int, k0: int, peak: float) -> dict:
+    """Each part timed on its own right after a read of 1 GiB, which leaves
+    no dirty line in the 129 MB L2: the part's own throughput, without the
+    write-back of the previous part's output that it absorbs inside a step
+    (CUDA events around the part only; outside the timed region of `value`)."""
+    import torch
+    flush = torch.ones(1 << 29, dtype=torch.float16, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in W.parts]
+    tot = [0.0] * len(W.parts)
+    for k in range(steps):
+        for i, p in enumerate(W.parts):
+            torch.sum(flush, dim=0, dtype=torch.float32, out=sink)
+            evs[i][0].record()
+            p.run(k0 + k)
+            evs[i][1].record()
+        torch.cuda.synchronize()
+        for i in range(len(W.parts)):
+            tot[i] += evs[i][0].elapsed_time(evs[i][1])
+    del flush
+    out = {}
+    for i, p in enumerate(W.parts):
+        ms = tot[i] / steps
+        gbs = p.bytes / (ms * 1e-3) / 1e9
+        out[p.name] = {"ms": round(ms, 5), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    return out
 
 
 def input_digests(W) -> dict:
