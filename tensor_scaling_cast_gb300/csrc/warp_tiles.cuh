@@ -199,15 +199,34 @@ __device__ __forceinline__ uint32_t mx_column(const uint32_t (&w)[32], uint32_t 
   return ebyte;
 }
 
+// L2 policy for stores whose 32-byte sectors are completed over a long
+// stretch of the kernel by many warps: evict-last keeps the partly written
+// lines in L2 until they are whole.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // The E8M0 bytes of one column for the row tiles i0 .. i0 + n - 1 of a chunk
 // (byte k of acc for row tile i0 + k), at e8 = the byte of row tile i0.  A
-// full chunk at an address aligned to its size goes out as one store.
+// full chunk at an address aligned to its size goes out as one store.  A
+// column's 32-byte sector of E8M0 bytes (32 row tiles) is filled by 32 / CH
+// chunks that different warps take at different times, so these stores
+// carry the evict-last policy: without it the partly written sectors were
+// evicted before they were complete (MX dual, OCP rule, bf16 [16384, 8192],
+// same box: 103.1 -> 98.3 us).
 template <int CH>
 using E8Acc = typename std::conditional<(CH > 4), unsigned long long, uint32_t>::type;
 template <int CH>
 __device__ __forceinline__ void store_e8_run(uint8_t* e8, E8Acc<CH> acc, uint32_t n) {
   if (n == (uint32_t)CH && (CH == 4 || CH == 8) && (reinterpret_cast<uintptr_t>(e8) & (CH - 1)) == 0) {
-    *reinterpret_cast<E8Acc<CH>*>(e8) = acc;
+    const uint64_t pol = l2_evict_last_policy();
+    if (CH == 4)
+      asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(e8), "r"((uint32_t)acc), "l"(pol) : "memory");
+    else
+      asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;" ::"l"(e8), "l"((unsigned long long)acc), "l"(pol)
+                   : "memory");
     return;
   }
   for (uint32_t k = 0; k < n; ++k) e8[k] = (uint8_t)(acc >> (8 * k));
