@@ -22,10 +22,10 @@ Besides the timed figures, each line carries `results` (what the
 configurations ask to report, computed with the library outside the timed
 region) and `inputs_sha256` (the SHA-256 of every input tensor's bytes), so
 the reported fractions can be tied to the exact inputs that produced them.
-Workloads of several parts also carry `parts_after_clean_l2`: each part
-timed alone after a read of 1 GiB that leaves no dirty line in L2, i.e.
-without the write-back of the previous part's output that a part absorbs
-inside a step (`parts`).
+Lines also carry `parts_after_clean_l2` (except the CUDA-graph workloads):
+each part timed alone after a read of 1 GiB that leaves no dirty line in
+L2, i.e. without the write-back of the previous part's (or step's) output
+that a part absorbs inside the timed steps (`parts`).
 """
 from __future__ import annotations
 
@@ -566,8 +566,7 @@ def run_ours(args, rank: int, world: int):
     dpart = parts[dom.name]
 
     copy_ref = copy_reference(dev, W.step_bytes)
-    clean = (parts_after_clean_l2(W, dev, min(K, 10), warm + K, peak)
-             if len(W.parts) > 1 and not W.graph_steps else None)
+    clean = parts_after_clean_l2(W, dev, min(K, 10), warm + K, peak) if not W.graph_steps else None
     results = workload_results(args.workload, dev) if rank == 0 else None
     digests = input_digests(W) if rank == 0 else None
     e2e = None
