@@ -36,20 +36,22 @@ namespace fp8q {
 // Pipeline shape of each kernel: TpCfg<input stages per warp, output
 // staging buffers per warp, row tiles per chunk, column-strip-first chunk
 // order, staging bytes, CTAs per SM (0: as many as fit), clip count, warps
-// per CTA>.  The cast + transpose moves little arithmetic per byte: it runs
-// one CTA of four warps per SM with six stages in flight per warp, which
-// keeps the read stream and its two write streams closer to the DRAM rate
-// than more, shallower warps do.  The MX dual carries much more arithmetic
-// per byte when its blocks may clip (the exact per-element count) and needs
-// the warps: twelve warps per SM (ten or fourteen measured slower), each
-// with three input stages and one staging buffer, which is what shared
-// memory allows, all in one CTA so that they work on twelve adjacent column
-// tiles (a CTA's warps on distant chunks cost 5%); a clip-free MX dual
-// (mx_clip_free) runs two CTAs of four three-stage warps per SM (one CTA of
-// eight measured 2.8% slower there).  Each shape was chosen by same-box
+// per CTA, count every block>.  The cast + transpose moves little arithmetic
+// per byte: it runs one CTA of four warps per SM with six stages in flight
+// per warp, which keeps the read stream and its two write streams closer to
+// the DRAM rate than more, shallower warps do.  The MX dual runs twelve
+// warps per SM (ten or fourteen measured slower), each with three input
+// stages and one staging buffer, which is what shared memory allows, all in
+// one CTA so that they work on twelve adjacent column tiles (a CTA's warps
+// on distant chunks cost 5%).  It counts the clipped elements of every block
+// without testing first whether the block can clip, under every rule: that
+// straight-line form measured faster than the guarded count, than a
+// clip-free kernel with no count, and than the guarded count on inputs where
+// no block clips (round-up rule 100.4 -> 97.6 us, OCP on such inputs
+// 103.8 -> 97.0 us, on tanh activations 97.8 -> 97.1 us; same box), and a
+// block that cannot clip adds 0.  Each shape was chosen by same-box
 // measurement on bf16 [16384, 8192].
-using DualCfg = TpCfg<3, 1, 4, true, 4096, 1, true, 12>;
-using DualClipFreeCfg = TpCfg<3, 2, 4, true, 4096, 2, false>;
+using DualCfg = TpCfg<3, 1, 4, true, 4096, 1, true, 12, true>;
 using CtCfg = TpCfg<6, 1, 4, true, 4096, 1>;
 constexpr int kTpL2Promotion = 128;      // bytes the L2 fetches per input-tile request
 
@@ -122,7 +124,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) mx_dual_kernel(
 #pragma unroll
         for (int k = 0; k < NG; ++k) t[k] = cast_load<DT, FMT>(v[k], s);
         pack_row<DT, NG>(t, o);
-        if (C::kClipCount && mx_block_may_clip<FMT>(m, E)) {
+        if (C::kClipCount && (C::kCountAll || mx_block_may_clip<FMT>(m, E))) {
 #pragma unroll
           for (int k = 0; k < 32; ++k)
             clip_r += clips<FMT>(__uint_as_float(elem_bits<DT>(v[k / EPL], k % EPL)) * s) ? 1u : 0u;
@@ -157,9 +159,9 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) mx_dual_kernel(
       if (c < cols) {
         load_column_words(tile, lane, w);
         const uint32_t pm = tree_absmax32<true>(w);
-        e8c0 |= (E8Acc<C::kChunk>)mx_column<FMT, 0, C::kClipCount>(w, pm << 16, rule, headroom, clip_c, o) << (8 * ci);
+        e8c0 |= (E8Acc<C::kChunk>)mx_column<FMT, 0, C::kClipCount, C::kCountAll>(w, pm << 16, rule, headroom, clip_c, o) << (8 * ci);
         stage32<32>(ob + 2048, 2 * lane, 0, o);
-        e8c1 |= (E8Acc<C::kChunk>)mx_column<FMT, 1, C::kClipCount>(w, pm & 0xFFFF0000u, rule, headroom, clip_c, o) << (8 * ci);
+        e8c1 |= (E8Acc<C::kChunk>)mx_column<FMT, 1, C::kClipCount, C::kCountAll>(w, pm & 0xFFFF0000u, rule, headroom, clip_c, o) << (8 * ci);
         stage32<32>(ob + 2048, 2 * lane + 1, 0, o);
         if (flush) {
           store_e8_run<C::kChunk>(e8_colt + c * rb + rt0, e8c0, ci + 1);
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) mx_dual_kernel(
       const int64_t c = c0 + lane;
       if (c < cols) {
         load_column_words(tile, lane, w);
-        e8c0 |= (E8Acc<C::kChunk>)mx_column<FMT, 2, C::kClipCount>(w, tree_absmax32<false>(w), rule, headroom, clip_c, o) << (8 * ci);
+        e8c0 |= (E8Acc<C::kChunk>)mx_column<FMT, 2, C::kClipCount, C::kCountAll>(w, tree_absmax32<false>(w), rule, headroom, clip_c, o) << (8 * ci);
         stage32<32>(ob + 2048, lane, 0, o);
         if (flush) store_e8_run<C::kChunk>(e8_colt + c * rb + rt0, e8c0, ci + 1);
       }
@@ -383,11 +385,8 @@ static cudaError_t launch_dual_t(const void* x, int64_t rows, int64_t cols, int 
                                  uint8_t* q_row, uint8_t* e8_row, uint8_t* q_colt, uint8_t* e8_colt,
                                  unsigned long long* cr, unsigned long long* cc, cudaStream_t s,
                                  int* launches) {
-  return mx_clip_free(rule, headroom)
-             ? launch_dual_c<DT, FMT, DualClipFreeCfg>(x, rows, cols, rule, headroom, q_row, e8_row, q_colt,
-                                                       e8_colt, cr, cc, s, launches)
-             : launch_dual_c<DT, FMT, DualCfg>(x, rows, cols, rule, headroom, q_row, e8_row, q_colt, e8_colt, cr,
-                                               cc, s, launches);
+  return launch_dual_c<DT, FMT, DualCfg>(x, rows, cols, rule, headroom, q_row, e8_row, q_colt, e8_colt, cr, cc, s,
+                                         launches);
 }
 
 cudaError_t launch_mx_dual(const void* x, int dtype, int64_t rows, int64_t cols, int format, int rule,

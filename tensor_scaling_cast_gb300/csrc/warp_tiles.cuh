@@ -32,11 +32,12 @@ constexpr int kWTileVec = kWTileBytes / 16;            // uint4 per sub-tile
 // buffers of OUTB bytes per warp, CH row tiles per chunk, chunk order, at
 // most MAXC resident CTAs per SM (0: as many as fit), whether the MX kernels
 // count clipped elements (CNT false only for clip-free casts, which cannot
-// clip), and W warps per CTA.  A CTA's warps start on W consecutive chunks
+// clip) and whether they count every block (ALL) or only the blocks whose
+// scaled maximum passes fmax, and W warps per CTA.  A CTA's warps start on W consecutive chunks
 // and advance together by the grid's warp count, so with column strips
 // first they always hold W adjacent column tiles of one row band: an SM
 // whose warps all sit in one CTA reads and writes one wide band at a time.
-template <int S, int OB, int CH, bool COLF, int OUTB, int MAXC = 0, bool CNT = true, int W = 4>
+template <int S, int OB, int CH, bool COLF, int OUTB, int MAXC = 0, bool CNT = true, int W = 4, bool ALL = false>
 struct TpCfg {
   static_assert(S >= 2 && S <= 8, "input stages");
   static_assert(OB == 1 || OB == 2, "one or two output staging buffers");
@@ -47,6 +48,7 @@ struct TpCfg {
   static constexpr bool kColFastest = COLF;      // chunk order: column tile fastest
   static constexpr int kMaxCtasPerSm = MAXC;
   static constexpr bool kClipCount = CNT;
+  static constexpr bool kCountAll = CNT && ALL;
   static constexpr int kWarps = W, kThreads = 32 * W;
   // launch bounds: CTAs per SM the register budget must allow (at most 128
   // registers a thread, fewer CTAs for wider ones)
@@ -175,10 +177,11 @@ __device__ __forceinline__ int staged_byte(int k, int b) {
 
 // One MX column block (column HI of the lane's words): its 32 bytes into o,
 // returns its E8M0 byte.  m = the block's max |x| bits.  With CNT the
-// block's clipped elements are added to clip (tested per element only when
-// its scaled max passes fmax); a clip-free cast (no CNT) has nothing to
-// count and carries no count code.
-template <int FMT, int HI, bool CNT>
+// block's clipped elements are added to clip, tested per element when its
+// scaled max passes fmax, or for every block with ALL (a block that cannot
+// clip adds 0); a clip-free cast (no CNT) has nothing to count and carries
+// no count code.
+template <int FMT, int HI, bool CNT, bool ALL = false>
 __device__ __forceinline__ uint32_t mx_column(const uint32_t (&w)[32], uint32_t m, int rule, int headroom,
                                               uint32_t& clip, uint32_t (&o)[8]) {
   uint32_t ebyte;
@@ -191,7 +194,7 @@ __device__ __forceinline__ uint32_t mx_column(const uint32_t (&w)[32], uint32_t 
     ebyte = (uint32_t)(E + 127);
     const float s = __uint_as_float((uint32_t)(127 - E) << 23);
     cast32<FMT, HI>(w, s, o);
-    if (CNT && mx_block_may_clip<FMT>(m, E)) {
+    if (CNT && (ALL || mx_block_may_clip<FMT>(m, E))) {
 #pragma unroll
       for (int k = 0; k < 32; ++k) clip += clips<FMT>(__uint_as_float(half_bits<HI>(w[k])) * s) ? 1u : 0u;
     }
